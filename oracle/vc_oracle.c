@@ -1,0 +1,503 @@
+/*
+ * vc_oracle.c -- plain, slow CPU oracle for the ExpCast-FP8 + V-Smooth FP8 attention forward.
+ *
+ * TEST INFRASTRUCTURE. This library exists only to check the CUDA path. Only the tests, the
+ * smoke check and the benchmark's CPU-baseline leg may load it; the product path never calls it.
+ * It shares no code, header, table or constant generator with the CUDA library.
+ *
+ * Sources, cited by page title and section/equation:
+ *   [VC]  "VC-Attention: Value Smoothing and Softmax Casting for Low-bit Attention" (arXiv 2609.15810)
+ *   [OVC] "Open-VC Attention: an open-source, error-tunable variant of VC-Attention" (MachGen blog)
+ *
+ * Floating point: sums, means and the exact attention are fp64. Where the method fixes an fp32
+ * step that decides an integer (the ExpCast code, an E4M3 code), the step is written in fp32 and
+ * the file must be compiled with -ffp-contract=off so that no a*b+c is fused behind our back.
+ *
+ * Readings taken where the pages are silent (each one also listed in the design notes):
+ *   R1  E4M3 follows the OCP FP8 E4M3 format the tensor core consumes: exponent field 0 is
+ *       subnormal (m/8 * 2^-6), 0x7F/0xFF are NaN, the largest finite value is 448.
+ *   R2  Encoding is round-to-nearest-even with saturation to +-448.
+ *   R3  One Q/K scale per 128-token block is one scalar over the 128 x D block, s = amax/448.
+ *   R4  k-means: Lloyd iterations (assign -> update) started from c_i = x_{floor(i*S/k)}; ties in
+ *       the assignment go to the lowest index; an empty cluster keeps its centroid.
+ *   R5  The partial last block's mean is taken over its valid rows only.
+ *   R6  The ExpCast pre-round value is computed as one fp32 fused multiply-add
+ *       y = fmaf(S32, a_j, 119.65f - M), then rounded to the nearest integer, ties to even, and
+ *       clipped to [0, 120]. Codes 1..7 decode as E4M3 subnormals.
+ *   R7  Key visit order for query tile qt: start = min(nkb-1, qt+2), sweep down to 0, then the tail.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_BLOCK 128
+
+/* ---------------------------------------------------------------------------------------------
+ * E4M3 codec.  [VC] §3.3: "A byte with exponent field e and mantissa field m encodes the value
+ * v = 2^(e-7)(1+m/8)".  Subnormals / NaN / saturation follow reading R1/R2.
+ * ------------------------------------------------------------------------------------------- */
+double orc_e4m3_decode(uint8_t c) {
+  int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  if (e == 15 && m == 7) return NAN;
+  double v = (e == 0) ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+  return sign ? -v : v;
+}
+
+uint8_t orc_e4m3_encode(float x) {
+  if (isnan(x)) return 0x7F;
+  uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  double a = fabs((double)x);
+  if (a > 448.0) return sign | 0x7E;
+  if (a < ldexp(1.0, -6)) {
+    /* subnormal grid: multiples of 2^-9; m == 8 lands exactly on the smallest normal (code 8) */
+    double m = nearbyint(a * 512.0);
+    return sign | (uint8_t)m;
+  }
+  int ex;
+  double fr = frexp(a, &ex);      /* a = fr * 2^ex, fr in [0.5, 1) */
+  int e = ex - 1;                 /* a = (2 fr) * 2^e, 2fr in [1, 2) */
+  double m = nearbyint((2.0 * fr - 1.0) * 8.0); /* exact product, RNE on the 3-bit mantissa */
+  if (m == 8.0) { e += 1; m = 0.0; }
+  int code = ((e + 7) << 3) | (int)m;
+  if (code > 0x7E) code = 0x7E;
+  return sign | (uint8_t)code;
+}
+
+void orc_e4m3_decode_n(const uint8_t* c, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_decode(c[i]);
+}
+void orc_e4m3_encode_n(const float* x, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_encode(x[i]);
+}
+
+/* bf16 helpers: bf16 -> fp32 is exact; fp64 -> bf16 rounds once, to nearest even. */
+static float bf16_to_f32(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+uint16_t orc_f64_to_bf16(double x) {
+  if (isnan(x)) return 0x7FC0;
+  uint16_t sign = signbit(x) ? 0x8000 : 0;
+  double a = fabs(x);
+  if (a == 0.0) return sign;
+  int ex;
+  double fr = frexp(a, &ex);      /* a = fr 2^ex, fr in [0.5,1) */
+  int e = ex - 1;                 /* unbiased exponent of a */
+  if (e < -126) {                 /* bf16 subnormal grid: multiples of 2^-133 */
+    double m = nearbyint(ldexp(a, 133));
+    uint32_t bits = (uint32_t)m;  /* m <= 128 -> may carry into the smallest normal */
+    return sign | (uint16_t)bits;
+  }
+  double m = nearbyint((2.0 * fr) * 128.0); /* 8 significant bits: [128, 256] */
+  if (m == 256.0) { m = 128.0; e += 1; }
+  if (e > 127) return sign | 0x7F80; /* overflow -> inf */
+  uint32_t bits = ((uint32_t)(e + 127) << 7) | ((uint32_t)m - 128u);
+  return sign | (uint16_t)bits;
+}
+void orc_f64_to_bf16_n(const double* x, int64_t n, uint16_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_f64_to_bf16(x[i]);
+}
+
+/* ---------------------------------------------------------------------------------------------
+ * ExpCast-FP8.  [VC] §3.3 Eq. 7: c(u) = clip_[0,120](Round(8(u+8) + 56 + beta)), beta = -0.35,
+ * Round = round-to-nearest-even.  [OVC] "Scheduling around ExpCast": the softmax scale, the Q/K
+ * dequantisation scales, log2 e, the factor 8 and the running maximum fold into one FMA a*S + b.
+ * With S32 the raw fp32 score and a_j = 8 log2(e)/sqrt(D) * sQ * sK, S32*a_j is the true score in
+ * code units, so 8(u+8)+56+beta = S32*a_j + (120 + beta) - M.  Reading R6 fixes the fp32 contract.
+ * ------------------------------------------------------------------------------------------- */
+static const float ORC_B0 = 119.65f; /* 8*8 + 56 + beta */
+
+int orc_expcast_unclipped(float s32, float a, float b) { return (int)rintf(fmaf(s32, a, b)); }
+
+int orc_expcast_code(float s32, float a, float b) {
+  float y = fmaf(s32, a, b);
+  if (isnan(y)) return 0;
+  float r = rintf(y);
+  if (r < 0.0f) return 0;
+  if (r > 120.0f) return 120;
+  return (int)r;
+}
+
+void orc_expcast_codes(const float* s, const float* a, const float* b, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = (uint8_t)orc_expcast_code(s[i], a[i], b[i]);
+}
+
+/* The conventional path that ExpCast replaces ([VC] §3.3, Fig. 5a): exponentiate, then cast to
+ * E4M3.  u is the log2-domain score relative to the row maximum; the row maximum lands at 2^8. */
+uint8_t orc_exp_then_cast(double u) { return orc_e4m3_encode((float)exp2(u + 8.0)); }
+
+/* Code of the direct map as a function of u alone (no fp32 score path): the reference formula
+ * of Eq. 7 evaluated in double, used by the pins that compare against the printed statistics. */
+int orc_expcast_of_u(double u) {
+  double r = nearbyint(8.0 * (u + 8.0) + 56.0 - 0.35);
+  if (r < 0) r = 0;
+  if (r > 120) r = 120;
+  return (int)r;
+}
+
+/* ---------------------------------------------------------------------------------------------
+ * Per-128-token block quantiser for Q and K'.  [OVC] "Scheduling around ExpCast": "Q and K are
+ * quantized to FP8 with one scale per 128-token block".  Reading R3: s = amax/448, inverse scale
+ * 448/amax computed once in fp32, code = E4M3(x * inv).  An all-zero block gets s = 1.
+ * x: [S, D] bf16 bits, codes: [S_pad, D] (pad rows zero), scales: [nkb].
+ * ------------------------------------------------------------------------------------------- */
+void orc_quant_blocks(const uint16_t* x, int64_t S, int D, uint8_t* codes, float* scales) {
+  int64_t nkb = (S + ORC_BLOCK - 1) / ORC_BLOCK;
+  memset(codes, 0, (size_t)(nkb * ORC_BLOCK * D));
+  for (int64_t j = 0; j < nkb; ++j) {
+    int64_t t0 = j * ORC_BLOCK, t1 = t0 + ORC_BLOCK < S ? t0 + ORC_BLOCK : S;
+    float amax = 0.0f;
+    for (int64_t t = t0; t < t1; ++t)
+      for (int d = 0; d < D; ++d) {
+        float v = fabsf(bf16_to_f32(x[t * D + d]));
+        if (v > amax) amax = v;
+      }
+    if (amax == 0.0f) { scales[j] = 1.0f; continue; }
+    float inv = 448.0f / amax;
+    scales[j] = amax / 448.0f;
+    for (int64_t t = t0; t < t1; ++t)
+      for (int d = 0; d < D; ++d) {
+        float v = bf16_to_f32(x[t * D + d]) * inv;
+        codes[t * D + d] = orc_e4m3_encode(v);
+      }
+  }
+}
+
+/* ---------------------------------------------------------------------------------------------
+ * Value-guided grouping.  [VC] §3.2 "Value-guided permutation": per batch and head an online
+ * k-means over the value tokens assigns a label z_t; pi = argsort(z); "Unbalanced clusters cost
+ * little": plain (unbalanced) k-means.  Reading R4 fixes init, iteration and ties.
+ * v: [S, D] bf16 bits.  labels: [S].  centroids: [k, D] (fp64).  J_rounds: [iters] objective of
+ * each round's assignment (sum of squared distances to the member means).
+ * ------------------------------------------------------------------------------------------- */
+double orc_kmeans_objective(const uint16_t* v, int64_t S, int D, int k, const int32_t* labels) {
+  double* sum = (double*)calloc((size_t)k * D, sizeof(double));
+  int64_t* cnt = (int64_t*)calloc((size_t)k, sizeof(int64_t));
+  for (int64_t t = 0; t < S; ++t) {
+    int z = labels[t];
+    cnt[z]++;
+    for (int d = 0; d < D; ++d) sum[(int64_t)z * D + d] += bf16_to_f32(v[t * D + d]);
+  }
+  for (int i = 0; i < k; ++i)
+    if (cnt[i])
+      for (int d = 0; d < D; ++d) sum[(int64_t)i * D + d] /= (double)cnt[i];
+  double J = 0.0;
+  for (int64_t t = 0; t < S; ++t) {
+    const double* m = sum + (int64_t)labels[t] * D;
+    for (int d = 0; d < D; ++d) {
+      double e = bf16_to_f32(v[t * D + d]) - m[d];
+      J += e * e;
+    }
+  }
+  free(sum);
+  free(cnt);
+  return J;
+}
+
+void orc_kmeans(const uint16_t* v, int64_t S, int D, int k, int iters, int32_t* labels, double* centroids,
+                double* J_rounds) {
+  for (int i = 0; i < k; ++i) {
+    int64_t src = (int64_t)((double)i * (double)S / (double)k);
+    for (int d = 0; d < D; ++d) centroids[(int64_t)i * D + d] = bf16_to_f32(v[src * D + d]);
+  }
+  double* sum = (double*)malloc((size_t)k * D * sizeof(double));
+  int64_t* cnt = (int64_t*)malloc((size_t)k * sizeof(int64_t));
+  for (int it = 0; it < iters; ++it) {
+    /* assign: nearest centroid in squared Euclidean distance, ties to the lowest index */
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < S; ++t) {
+      double best = INFINITY;
+      int bi = 0;
+      for (int i = 0; i < k; ++i) {
+        const double* c = centroids + (int64_t)i * D;
+        double dist = 0.0;
+        for (int d = 0; d < D; ++d) {
+          double e = (double)bf16_to_f32(v[t * D + d]) - c[d];
+          dist += e * e;
+        }
+        if (dist < best) { best = dist; bi = i; }
+      }
+      labels[t] = bi;
+    }
+    if (J_rounds) J_rounds[it] = orc_kmeans_objective(v, S, D, k, labels);
+    /* update: member mean; an empty cluster keeps its centroid */
+    memset(sum, 0, (size_t)k * D * sizeof(double));
+    memset(cnt, 0, (size_t)k * sizeof(int64_t));
+    for (int64_t t = 0; t < S; ++t) {
+      cnt[labels[t]]++;
+      for (int d = 0; d < D; ++d) sum[(int64_t)labels[t] * D + d] += bf16_to_f32(v[t * D + d]);
+    }
+    for (int i = 0; i < k; ++i)
+      if (cnt[i])
+        for (int d = 0; d < D; ++d) centroids[(int64_t)i * D + d] = sum[(int64_t)i * D + d] / (double)cnt[i];
+  }
+  free(sum);
+  free(cnt);
+}
+
+/* Stable argsort of the labels by counting sort: pi lists the tokens of cluster 0 in token order,
+ * then cluster 1, ...  ([VC] §3.2 Eq. 3: pi = argsort(z), applied to K and V, Q keeps its order.) */
+void orc_stable_argsort(const int32_t* z, int64_t S, int k, int32_t* perm) {
+  int64_t* start = (int64_t*)calloc((size_t)k + 1, sizeof(int64_t));
+  for (int64_t t = 0; t < S; ++t) start[z[t] + 1]++;
+  for (int i = 0; i < k; ++i) start[i + 1] += start[i];
+  for (int64_t t = 0; t < S; ++t) perm[start[z[t]]++] = (int32_t)t;
+  free(start);
+}
+
+/* ---------------------------------------------------------------------------------------------
+ * Gather, block demeaning and residual quantisation of V.  [VC] §3.2 "Block demeaning" Eq. 4:
+ * mu_j = mean of the rows of block j of V' = V[pi], R_j = V'_j - 1 mu_j^T, each mean one 16-bit
+ * vector.  [OVC] "Scheduling around ExpCast": V (here its residual) gets one scale per head.
+ * The residual is taken against the stored bf16 mean, so R + mu_b reconstructs V' (reading R5 for
+ * the partial block).  perm may be NULL (identity); subtract_mean = 0 gives R = V' and mu = 0.
+ * Outputs: mu [nkb, D] fp64 (exact mean), mub [nkb, D] bf16 bits, resid [S_pad, D] fp32 (pad rows
+ * zero), rcodes [S_pad, D] E4M3 codes of R * 448/amax, *amax_out, *sv_out = amax/448.
+ * ------------------------------------------------------------------------------------------- */
+void orc_demean(const uint16_t* v, const int32_t* perm, int64_t S, int D, int subtract_mean, double* mu,
+                uint16_t* mub, float* resid, uint8_t* rcodes, float* amax_out, float* sv_out) {
+  int64_t nkb = (S + ORC_BLOCK - 1) / ORC_BLOCK;
+  memset(resid, 0, (size_t)(nkb * ORC_BLOCK * D) * sizeof(float));
+  memset(rcodes, 0, (size_t)(nkb * ORC_BLOCK * D));
+  float amax = 0.0f;
+  for (int64_t j = 0; j < nkb; ++j) {
+    int64_t t0 = j * ORC_BLOCK, t1 = t0 + ORC_BLOCK < S ? t0 + ORC_BLOCK : S;
+    for (int d = 0; d < D; ++d) {
+      double s = 0.0;
+      for (int64_t t = t0; t < t1; ++t) {
+        int64_t src = perm ? perm[t] : t;
+        s += bf16_to_f32(v[src * D + d]);
+      }
+      double m = subtract_mean ? s / (double)(t1 - t0) : 0.0;
+      mu[j * D + d] = m;
+      mub[j * D + d] = orc_f64_to_bf16(m);
+    }
+    for (int64_t t = t0; t < t1; ++t) {
+      int64_t src = perm ? perm[t] : t;
+      for (int d = 0; d < D; ++d) {
+        float r = bf16_to_f32(v[src * D + d]) - bf16_to_f32(mub[j * D + d]);
+        resid[t * D + d] = r;
+        if (fabsf(r) > amax) amax = fabsf(r);
+      }
+    }
+  }
+  float inv = amax > 0.0f ? 448.0f / amax : 1.0f;
+  float sv = amax > 0.0f ? amax / 448.0f : 1.0f;
+  for (int64_t t = 0; t < S; ++t)
+    for (int d = 0; d < D; ++d) rcodes[t * D + d] = orc_e4m3_encode(resid[t * D + d] * inv);
+  *amax_out = amax;
+  *sv_out = sv;
+}
+
+/* Gather rows of a [S, D] bf16 tensor by pi: out[t] = x[pi[t]]  ([VC] §3.2 Eq. 3: K' = K[pi]). */
+void orc_gather_rows(const uint16_t* x, const int32_t* perm, int64_t S, int D, uint16_t* out) {
+  for (int64_t t = 0; t < S; ++t) memcpy(out + t * D, x + (int64_t)perm[t] * D, (size_t)D * 2);
+}
+
+/* ---------------------------------------------------------------------------------------------
+ * Key visit order.  [OVC] "Scheduling around ExpCast", mid-window key traversal: start a few
+ * blocks past the query's diagonal block, sweep down to block 0, then visit the tail; every block
+ * once.  Reading R7: "a few" = 2.  midwindow = 0 gives the linear order 0..nkb-1.
+ * ------------------------------------------------------------------------------------------- */
+void orc_visit_order(int nkb, int qt, int midwindow, int32_t* order) {
+  if (!midwindow) {
+    for (int i = 0; i < nkb; ++i) order[i] = i;
+    return;
+  }
+  int start = qt + 2 < nkb - 1 ? qt + 2 : nkb - 1;
+  int n = 0;
+  for (int j = start; j >= 0; --j) order[n++] = j;
+  for (int j = start + 1; j < nkb; ++j) order[n++] = j;
+}
+
+/* ---------------------------------------------------------------------------------------------
+ * (i) The quantised attention forward, one query row at a time.
+ *   [VC] §3.1 Eq. 1 (online softmax), §3.2 Eq. 6 (online mean restoration
+ *   A <- alpha A + P~ R_q + r mu^T, l <- alpha l + r, r = P~ 1), §3.3 Eq. 7 (ExpCast);
+ *   [OVC] "Scheduling around ExpCast": running max on the true score, every increase applied with
+ *   an output rescale, row sum of the decoded FP8 probabilities that feed PV, mid-window order.
+ * Inputs (one batch-head): qc,kc,rc [S_pad, D] E4M3 codes (K and R already permuted), sq,sk [nkb],
+ * sv the per-head residual scale, mub [nkb, D] bf16 means (NULL: no mean term).
+ * flags: 1 = ExpCast (else exponentiate then cast), 2 = mid-window order (else linear).
+ * rows: query token indices.  Outputs per row: out [D] fp64 = sv*A/l, l, final max M (code units).
+ * ------------------------------------------------------------------------------------------- */
+#define ORC_EXPCAST 1
+#define ORC_MIDWINDOW 2
+
+float orc_code_scale(int D) { return (float)(8.0 * 1.4426950408889634 / sqrt((double)D)); }
+
+void orc_attention_quant(const uint8_t* qc, const float* sq, const uint8_t* kc, const float* sk, const uint8_t* rc,
+                         float sv, const uint16_t* mub, int64_t S, int D, int flags, const int64_t* rows,
+                         int64_t nrows, double* out, double* l_out, float* m_out) {
+  int nkb = (int)((S + ORC_BLOCK - 1) / ORC_BLOCK);
+  float C = orc_code_scale(D);
+#pragma omp parallel
+  {
+    int32_t* order = (int32_t*)malloc((size_t)nkb * sizeof(int32_t));
+    double* A = (double*)malloc((size_t)D * sizeof(double));
+    double* qd = (double*)malloc((size_t)D * sizeof(double));
+    float s32[ORC_BLOCK];
+    uint8_t code[ORC_BLOCK];
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t ri = 0; ri < nrows; ++ri) {
+      int64_t r = rows[ri];
+      int qt = (int)(r / ORC_BLOCK);
+      orc_visit_order(nkb, qt, flags & ORC_MIDWINDOW, order);
+      for (int d = 0; d < D; ++d) qd[d] = orc_e4m3_decode(qc[r * D + d]);
+      float aq = C * sq[qt];
+      float M = -INFINITY;
+      double l = 0.0;
+      for (int d = 0; d < D; ++d) A[d] = 0.0;
+      for (int oi = 0; oi < nkb; ++oi) {
+        int j = order[oi];
+        int ncols = (int)((int64_t)(j + 1) * ORC_BLOCK <= S ? ORC_BLOCK : S - (int64_t)j * ORC_BLOCK);
+        float aj = aq * sk[j];
+        /* raw score: exact in fp64 (at most 50 significant bits), then one rounding to fp32 */
+        float t = -INFINITY;
+        for (int c = 0; c < ncols; ++c) {
+          const uint8_t* kr = kc + ((int64_t)j * ORC_BLOCK + c) * D;
+          double acc = 0.0;
+          for (int d = 0; d < D; ++d) acc += qd[d] * orc_e4m3_decode(kr[d]);
+          s32[c] = (float)acc;
+          float sc = s32[c] * aj;
+          if (sc > t) t = sc;
+        }
+        float Mn = M > t ? M : t;
+        if (Mn > M && M > -INFINITY) {
+          double alpha = exp2(((double)M - (double)Mn) / 8.0);
+          for (int d = 0; d < D; ++d) A[d] *= alpha;
+          l *= alpha;
+        }
+        M = Mn;
+        float b = ORC_B0 - M;
+        double rj = 0.0;
+        for (int c = 0; c < ncols; ++c) {
+          if (flags & ORC_EXPCAST) {
+            code[c] = (uint8_t)orc_expcast_code(s32[c], aj, b);
+          } else {
+            float y = fmaf(s32[c], aj, b);
+            float ze = (y - ORC_B0) * 0.125f + 8.0f;
+            code[c] = orc_e4m3_encode((float)exp2((double)ze));
+          }
+          rj += orc_e4m3_decode(code[c]);
+        }
+        for (int d = 0; d < D; ++d) {
+          double acc = 0.0;
+          for (int c = 0; c < ncols; ++c)
+            acc += orc_e4m3_decode(code[c]) * orc_e4m3_decode(rc[((int64_t)j * ORC_BLOCK + c) * D + d]);
+          double mean_term = mub ? rj * ((double)bf16_to_f32(mub[(int64_t)j * D + d]) / (double)sv) : 0.0;
+          A[d] += acc + mean_term;
+        }
+        l += rj;
+      }
+      for (int d = 0; d < D; ++d) out[ri * D + d] = (double)sv * A[d] / l;
+      if (l_out) l_out[ri] = l;
+      if (m_out) m_out[ri] = M;
+    }
+    free(order);
+    free(A);
+    free(qd);
+  }
+}
+
+/* ---------------------------------------------------------------------------------------------
+ * (ii) Exact softmax attention in fp64 on the unquantised, unpermuted inputs.
+ * [VC] §3.1: S = Q K^T / sqrt(d), P = softmax(S), O = P V.  q,k,v: [S, D] bf16 bits.
+ * ------------------------------------------------------------------------------------------- */
+void orc_attention_exact(const uint16_t* q, const uint16_t* k, const uint16_t* v, int64_t S, int D,
+                         const int64_t* rows, int64_t nrows, double* out) {
+  double scale = 1.0 / sqrt((double)D);
+#pragma omp parallel
+  {
+    double* s = (double*)malloc((size_t)S * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t ri = 0; ri < nrows; ++ri) {
+      int64_t r = rows[ri];
+      double mx = -INFINITY;
+      for (int64_t t = 0; t < S; ++t) {
+        double acc = 0.0;
+        for (int d = 0; d < D; ++d) acc += (double)bf16_to_f32(q[r * D + d]) * (double)bf16_to_f32(k[t * D + d]);
+        s[t] = acc * scale;
+        if (s[t] > mx) mx = s[t];
+      }
+      double den = 0.0;
+      for (int64_t t = 0; t < S; ++t) {
+        s[t] = exp(s[t] - mx);
+        den += s[t];
+      }
+      for (int d = 0; d < D; ++d) {
+        double acc = 0.0;
+        for (int64_t t = 0; t < S; ++t) acc += s[t] * (double)bf16_to_f32(v[t * D + d]);
+        out[ri * D + d] = acc / den;
+      }
+    }
+    free(s);
+  }
+}
+
+/* ---------------------------------------------------------------------------------------------
+ * The same tiled recurrence with every quantiser switched off, for the mean-restoration check of
+ * [VC] §3.2 "Online mean restoration": scores exact (fp64, natural-log domain), probabilities the
+ * exact exp, V' = R + 1 mu^T with R and mu kept in fp64.  It must reproduce (ii) to rounding.
+ * q,k,v: [S, D] fp64 (K, V already permuted), perm unused here.
+ * ------------------------------------------------------------------------------------------- */
+void orc_attention_demeaned_exact(const double* q, const double* k, const double* v, int64_t S, int D, int flags,
+                                  const int64_t* rows, int64_t nrows, double* out) {
+  int nkb = (int)((S + ORC_BLOCK - 1) / ORC_BLOCK);
+  double scale = 1.0 / sqrt((double)D);
+  double* mu = (double*)malloc((size_t)nkb * D * sizeof(double));
+  for (int j = 0; j < nkb; ++j) {
+    int64_t t0 = (int64_t)j * ORC_BLOCK, t1 = t0 + ORC_BLOCK < S ? t0 + ORC_BLOCK : S;
+    for (int d = 0; d < D; ++d) {
+      double s = 0.0;
+      for (int64_t t = t0; t < t1; ++t) s += v[t * D + d];
+      mu[j * D + d] = s / (double)(t1 - t0);
+    }
+  }
+#pragma omp parallel
+  {
+    int32_t* order = (int32_t*)malloc((size_t)nkb * sizeof(int32_t));
+    double* A = (double*)malloc((size_t)D * sizeof(double));
+    double p[ORC_BLOCK];
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t ri = 0; ri < nrows; ++ri) {
+      int64_t r = rows[ri];
+      orc_visit_order(nkb, (int)(r / ORC_BLOCK), flags & ORC_MIDWINDOW, order);
+      double m = -INFINITY, l = 0.0;
+      for (int d = 0; d < D; ++d) A[d] = 0.0;
+      for (int oi = 0; oi < nkb; ++oi) {
+        int j = order[oi];
+        int ncols = (int)((int64_t)(j + 1) * ORC_BLOCK <= S ? ORC_BLOCK : S - (int64_t)j * ORC_BLOCK);
+        double tmax = -INFINITY;
+        for (int c = 0; c < ncols; ++c) {
+          double acc = 0.0;
+          for (int d = 0; d < D; ++d) acc += q[r * D + d] * k[((int64_t)j * ORC_BLOCK + c) * D + d];
+          p[c] = acc * scale;
+          if (p[c] > tmax) tmax = p[c];
+        }
+        double mn = m > tmax ? m : tmax;
+        double alpha = (m == -INFINITY) ? 0.0 : exp(m - mn);
+        double rj = 0.0;
+        for (int c = 0; c < ncols; ++c) {
+          p[c] = exp(p[c] - mn);
+          rj += p[c];
+        }
+        for (int d = 0; d < D; ++d) {
+          double acc = 0.0;
+          for (int c = 0; c < ncols; ++c)
+            acc += p[c] * (v[((int64_t)j * ORC_BLOCK + c) * D + d] - mu[(int64_t)j * D + d]);
+          A[d] = alpha * A[d] + acc + rj * mu[(int64_t)j * D + d];
+        }
+        l = alpha * l + rj;
+        m = mn;
+      }
+      for (int d = 0; d < D; ++d) out[ri * D + d] = A[d] / l;
+    }
+    free(order);
+    free(A);
+  }
+  free(mu);
+}
