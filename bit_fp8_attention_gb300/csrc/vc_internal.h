@@ -1,0 +1,42 @@
+// vc_internal.h -- definitions shared by the library's translation units (not part of the ABI).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/vc_attn.h"
+
+namespace vc {
+
+// Device buffers of a plan (layouts as documented in vc_attn.h).
+struct PlanBuffers {
+  int B, H, S, D, k, nkb, S_pad;
+  uint8_t* qcodes;      // [BH, S_pad, D]
+  float* qscales;       // [BH, nkb]
+  uint8_t* kcodes;      // [BH, S_pad, D]
+  float* kscales;       // [BH, nkb]
+  uint8_t* vcodes;      // [BH, D, S_pad]
+  float* vscales;       // [BH]
+  uint16_t* means;      // [BH, nkb, D] bf16
+  int32_t* labels;      // [BH, S]
+  int32_t* perm;        // [BH, S]
+  float* cent;          // [BH, k, D]
+  float* cnorm;         // [BH, k]
+  int32_t* counts;      // [BH, k]
+  int32_t* offsets;     // [BH, k]
+  unsigned int* vamax;  // [BH] residual |max| as float bits
+  int* status;          // [1]
+  bool has_means;       // prepared with V-Smooth
+};
+
+int prepare_launch(const PlanBuffers& p, const uint16_t* Q, const uint16_t* K, const uint16_t* V,
+                   const int32_t* perm_in, bool vsmooth, int iters, cudaStream_t st);
+
+struct FwdMaps {
+  CUtensorMap q, k, v;
+};
+int encode_fwd_maps(const PlanBuffers& p, FwdMaps* maps);
+int forward_launch(const PlanBuffers& p, const FwdMaps& maps, uint16_t* O, unsigned flags, cudaStream_t st);
+int expcast_launch(const float* s, const float* a, const float* b, int64_t n, uint8_t* out, cudaStream_t st);
+
+}  // namespace vc

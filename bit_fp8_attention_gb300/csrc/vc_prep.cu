@@ -1,0 +1,486 @@
+// vc_prep.cu -- the prepare step on the GPU: per-128-token block quantisation of Q and K',
+// k-means over V rows with a stable counting-sort argsort, gather of K and V by the permutation,
+// bf16 block means, and the per-head residual quantisation packed transposed for the PV operand.
+//
+// "VC-Attention: Value Smoothing and Softmax Casting for Low-bit Attention", Sec. 3.2
+// ("Value-guided permutation" Eq. 3, "Block demeaning" Eq. 4, "Unbalanced clusters cost little"),
+// Sec. 3.4 "Fused preprocessing"; "Open-VC Attention" (MachGen blog), "Scheduling around ExpCast"
+// (one scale per 128-token Q/K block, one V scale per head) and "Packed V" ([H, D, S_pad], key
+// dimension contiguous).  All of these passes are memory-bound except the k-means assignment.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "vc_device.cuh"
+#include "vc_internal.h"
+
+namespace vc {
+
+static __device__ __forceinline__ float bf16_bits_to_f32(uint32_t h16) { return __uint_as_float(h16 << 16); }
+
+// Round a double to bf16, to nearest even, in one step (no intermediate fp32 rounding).
+static __device__ uint16_t f64_to_bf16_rne(double x) {
+  uint64_t u = (uint64_t)__double_as_longlong(x);
+  uint16_t sign = (uint16_t)((u >> 48) & 0x8000u);
+  uint64_t mag = u & 0x7FFFFFFFFFFFFFFFull;
+  if (mag == 0) return sign;
+  if (mag >= 0x7FF0000000000000ull) return sign | (mag > 0x7FF0000000000000ull ? 0x7FC0 : 0x7F80);
+  int e = (int)(mag >> 52) - 1023;  // unbiased exponent (normal doubles only in practice)
+  uint64_t m = (mag & 0xFFFFFFFFFFFFFull) | (1ull << 52);
+  if (e < -126) {
+    // bf16 subnormal: value = q * 2^-133 with q = rne(x * 2^133)
+    int shift = 52 - (e + 133);  // bits of m below the 2^-133 position
+    if (shift > 63) return sign;
+    uint64_t q = m >> shift;
+    uint64_t rem = m & ((1ull << shift) - 1), half = 1ull << (shift - 1);
+    if (rem > half || (rem == half && (q & 1))) ++q;
+    return sign | (uint16_t)q;  // q <= 128 (128 is the smallest normal)
+  }
+  uint64_t q = m >> 45;  // 8 significant bits
+  uint64_t rem = m & ((1ull << 45) - 1), half = 1ull << 44;
+  if (rem > half || (rem == half && (q & 1))) ++q;
+  if (q == 256) { q = 128; ++e; }
+  if (e > 127) return sign | 0x7F80;
+  return sign | (uint16_t)(((uint32_t)(e + 127) << 7) | ((uint32_t)q - 128u));
+}
+
+// ---------------------------------------------------------------------------------------------
+// Block quantiser.  One CTA per (128-token block j, batch-head bh).  Rows are read through `perm`
+// when it is given (the K' = K[pi] gather), otherwise in order.  amax over the whole 128 x D
+// block, scale = amax/448, code = E4M3_rne_satfinite(x * (448/amax)); pad rows get code 0.
+// ---------------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) quant_blocks_kernel(const uint16_t* __restrict__ x,
+                                                           const int32_t* __restrict__ perm, int S, int S_pad,
+                                                           uint8_t* __restrict__ codes, float* __restrict__ scales) {
+  constexpr int CPR = D / 8;                 // 16-byte chunks per row
+  constexpr int NCH = 128 * CPR / 256;       // chunks per thread
+  const int j = blockIdx.x, bh = blockIdx.y;
+  const int nkb = S_pad / 128;
+  const uint16_t* xh = x + (int64_t)bh * S * D;
+  const int32_t* ph = perm ? perm + (int64_t)bh * S : nullptr;
+  uint4 v[NCH];
+  float amax = 0.f;
+#pragma unroll
+  for (int m = 0; m < NCH; ++m) {
+    int c = threadIdx.x + 256 * m;
+    int r = c / CPR, cc = c % CPR;
+    int t = j * 128 + r;
+    if (t < S) {
+      int src = ph ? ph[t] : t;
+      v[m] = *reinterpret_cast<const uint4*>(xh + (int64_t)src * D + cc * 8);
+    } else {
+      v[m] = make_uint4(0, 0, 0, 0);
+    }
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(&v[m]);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w[q] & 0xFFFFu)));
+      amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w[q] >> 16)));
+    }
+  }
+  __shared__ float red[8];
+#pragma unroll
+  for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+  const bool zero = !(amax > 0.f);
+  const float inv = zero ? 0.f : __fdiv_rn(448.f, amax);
+  if (threadIdx.x == 0) scales[(int64_t)bh * nkb + j] = zero ? 1.f : __fdiv_rn(amax, 448.f);
+  uint8_t* ch = codes + ((int64_t)bh * S_pad + (int64_t)j * 128) * D;
+#pragma unroll
+  for (int m = 0; m < NCH; ++m) {
+    int c = threadIdx.x + 256 * m;
+    int r = c / CPR, cc = c % CPR;
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(&v[m]);
+    uint32_t lo = 0, hi = 0;
+    if (!zero) {
+      lo = cvt_e4m3x2(__fmul_rn(bf16_bits_to_f32(w[0] & 0xFFFFu), inv), __fmul_rn(bf16_bits_to_f32(w[0] >> 16), inv)) |
+           (cvt_e4m3x2(__fmul_rn(bf16_bits_to_f32(w[1] & 0xFFFFu), inv), __fmul_rn(bf16_bits_to_f32(w[1] >> 16), inv))
+            << 16);
+      hi = cvt_e4m3x2(__fmul_rn(bf16_bits_to_f32(w[2] & 0xFFFFu), inv), __fmul_rn(bf16_bits_to_f32(w[2] >> 16), inv)) |
+           (cvt_e4m3x2(__fmul_rn(bf16_bits_to_f32(w[3] & 0xFFFFu), inv), __fmul_rn(bf16_bits_to_f32(w[3] >> 16), inv))
+            << 16);
+    }
+    *reinterpret_cast<uint2*>(ch + (int64_t)r * D + cc * 8) = make_uint2(lo, hi);
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// k-means.  Reading of "online k-means" (VC-Attention Sec. 3.2): Lloyd rounds run at inference
+// time; centroids start at the rows floor(i*S/k); assignment to the nearest centroid in squared
+// Euclidean distance (evaluated as ||c||^2 - 2 x.c in fp32; near-ties may resolve differently
+// from an fp64 evaluation); update = member mean (fp64 sums), an empty cluster keeps its centroid.
+// ---------------------------------------------------------------------------------------------
+__global__ void kmeans_init_kernel(const uint16_t* __restrict__ v, int S, int D, int k, float* __restrict__ cent,
+                                   float* __restrict__ cnorm) {
+  const int i = blockIdx.x, bh = blockIdx.y;
+  const int64_t src = (int64_t)i * S / k;
+  const uint16_t* row = v + ((int64_t)bh * S + src) * D;
+  float* c = cent + ((int64_t)bh * k + i) * D;
+  float acc = 0.f;
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float x = bf16_bits_to_f32(row[d]);
+    c[d] = x;
+    acc = fmaf(x, x, acc);
+  }
+  __shared__ float red[32];
+  for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float s = 0.f;
+    for (int w = 0; w < (int)(blockDim.x + 31) / 32; ++w) s += red[w];
+    cnorm[(int64_t)bh * k + i] = s;
+  }
+}
+
+// Tile: 64 tokens x 64 centroids per step, 256 threads, 4 x 4 register tile per thread.
+template <int D>
+constexpr int kmeans_assign_smem() { return (D * (64 + 4) * 2 + 16 * 64 * 2) * 4; }
+
+template <int D>
+__global__ void __launch_bounds__(256) kmeans_assign_kernel(const uint16_t* __restrict__ v, int S, int k,
+                                                            const float* __restrict__ cent,
+                                                            const float* __restrict__ cnorm,
+                                                            int32_t* __restrict__ labels) {
+  constexpr int TT = 64, TC = 64;
+  extern __shared__ float kmeans_smem[];
+  float(*xs)[TT + 4] = reinterpret_cast<float(*)[TT + 4]>(kmeans_smem);            // xs[d][token]
+  float(*cs)[TC + 4] = reinterpret_cast<float(*)[TC + 4]>(kmeans_smem + D * (TT + 4));  // cs[d][centroid]
+  float(*bestd)[TT] = reinterpret_cast<float(*)[TT]>(kmeans_smem + D * (TT + 4) + D * (TC + 4));
+  int(*besti)[TT] = reinterpret_cast<int(*)[TT]>(kmeans_smem + D * (TT + 4) + D * (TC + 4) + 16 * TT);
+  const int bh = blockIdx.y;
+  const int t0 = blockIdx.x * TT;
+  const int tid = threadIdx.x;
+  const int tr = tid / 16, tc = tid % 16;  // token group (4 tokens), centroid group (4 centroids)
+  const uint16_t* vh = v + (int64_t)bh * S * D;
+  for (int e = tid; e < TT * D; e += 256) {
+    int r = e / D, d = e % D;
+    int t = t0 + r;
+    xs[d][r] = t < S ? bf16_bits_to_f32(vh[(int64_t)t * D + d]) : 0.f;
+  }
+  float bd[4];
+  int bi[4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) { bd[a] = INFINITY; bi[a] = 0; }
+  const float* ch = cent + (int64_t)bh * k * D;
+  const float* nh = cnorm + (int64_t)bh * k;
+  for (int c0 = 0; c0 < k; c0 += TC) {
+    __syncthreads();
+    for (int e = tid; e < TC * D; e += 256) {
+      int r = e / D, d = e % D;
+      cs[d][r] = (c0 + r) < k ? ch[(int64_t)(c0 + r) * D + d] : 0.f;
+    }
+    __syncthreads();
+    float acc[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+#pragma unroll 8
+    for (int d = 0; d < D; ++d) {
+      float xa[4], cb[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) xa[a] = xs[d][tr * 4 + a];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) cb[b] = cs[d][tc * 4 + b];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(xa[a], cb[b], acc[a][b]);
+    }
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      int ci = c0 + tc * 4 + b;
+      if (ci < k) {
+        float cn = nh[ci];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          float dist = fmaf(-2.f, acc[a][b], cn);
+          if (dist < bd[a]) { bd[a] = dist; bi[a] = ci; }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    bestd[tc][tr * 4 + a] = bd[a];
+    besti[tc][tr * 4 + a] = bi[a];
+  }
+  __syncthreads();
+  if (tid < TT) {
+    float b = bestd[0][tid];
+    int i = besti[0][tid];
+    for (int g = 1; g < 16; ++g) {  // lexicographic (distance, index): ties go to the lowest index
+      float d2 = bestd[g][tid];
+      int i2 = besti[g][tid];
+      if (d2 < b || (d2 == b && i2 < i)) { b = d2; i = i2; }
+    }
+    int t = t0 + tid;
+    if (t < S) labels[(int64_t)bh * S + t] = i;
+  }
+}
+
+// Stable counting sort of the labels of one batch-head: counts, exclusive offsets, and the
+// permutation listing cluster 0's tokens in token order, then cluster 1's, ...
+__global__ void __launch_bounds__(1024) argsort_kernel(const int32_t* __restrict__ labels, int S, int k,
+                                                       int32_t* __restrict__ perm, int32_t* __restrict__ counts,
+                                                       int32_t* __restrict__ offsets) {
+  __shared__ int hist[1024];
+  __shared__ int off[1024];
+  const int bh = blockIdx.x;
+  const int32_t* z = labels + (int64_t)bh * S;
+  for (int i = threadIdx.x; i < k; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  for (int t = threadIdx.x; t < S; t += blockDim.x) atomicAdd(&hist[z[t]], 1);
+  __syncthreads();
+  if (threadIdx.x < 32) {  // exclusive scan by one warp over k <= 1024 entries
+    int carry = 0;
+    for (int base = 0; base < k; base += 32) {
+      int i = base + threadIdx.x;
+      int val = i < k ? hist[i] : 0;
+      int incl = val;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if ((int)threadIdx.x >= o) incl += n;
+      }
+      if (i < k) off[i] = carry + incl - val;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < k; i += blockDim.x) {
+    counts[(int64_t)bh * k + i] = hist[i];
+    offsets[(int64_t)bh * k + i] = off[i];
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {  // one warp scatters in token order, 32 tokens at a time
+    const unsigned lane = threadIdx.x;
+    int32_t* p = perm + (int64_t)bh * S;
+    for (int base = 0; base < S; base += 32) {
+      int t = base + (int)lane;
+      bool act = t < S;
+      int zz = act ? z[t] : -1 - (int)lane;  // inactive lanes get unique keys
+      unsigned peers = __match_any_sync(0xffffffffu, zz);
+      int rank = __popc(peers & ((1u << lane) - 1u));
+      int pos = act ? off[zz] + rank : 0;
+      __syncwarp();
+      if (act) {
+        p[pos] = t;
+        if (rank == 0) off[zz] += __popc(peers);
+      }
+      __syncwarp();
+    }
+  }
+}
+
+// Member means, one CTA per (cluster, batch-head); fp64 column sums over the cluster's tokens.
+__global__ void kmeans_update_kernel(const uint16_t* __restrict__ v, int S, int D, int k,
+                                     const int32_t* __restrict__ perm, const int32_t* __restrict__ counts,
+                                     const int32_t* __restrict__ offsets, float* __restrict__ cent,
+                                     float* __restrict__ cnorm) {
+  const int i = blockIdx.x, bh = blockIdx.y;
+  const int n = counts[(int64_t)bh * k + i];
+  const int o = offsets[(int64_t)bh * k + i];
+  const uint16_t* vh = v + (int64_t)bh * S * D;
+  const int32_t* ph = perm + (int64_t)bh * S;
+  float* c = cent + ((int64_t)bh * k + i) * D;
+  __shared__ float red[32];
+  float nrm = 0.f;
+  if (n > 0) {
+    for (int d = threadIdx.x; d < D; d += blockDim.x) {
+      double s = 0.0;
+      for (int m = 0; m < n; ++m) s += (double)bf16_bits_to_f32(vh[(int64_t)ph[o + m] * D + d]);
+      float cv = (float)(s / (double)n);
+      c[d] = cv;
+      nrm = fmaf(cv, cv, nrm);
+    }
+  } else {
+    for (int d = threadIdx.x; d < D; d += blockDim.x) nrm = fmaf(c[d], c[d], nrm);
+  }
+  for (int off = 16; off; off >>= 1) nrm += __shfl_xor_sync(0xffffffffu, nrm, off);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = nrm;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float s = 0.f;
+    for (int w = 0; w < (int)(blockDim.x + 31) / 32; ++w) s += red[w];
+    cnorm[(int64_t)bh * k + i] = s;
+  }
+}
+
+__global__ void iota_kernel(int32_t* __restrict__ perm, int S, int64_t total) {
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < total) perm[i] = (int32_t)(i % S);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Block means of V' = V[pi] and the per-head residual maximum.  One CTA per (block, bh).
+// mu_j = (sum of the valid rows, exact in fp64) / n_j, rounded once to bf16; R = V' - mu_b in
+// fp32; amax_h = max |R| over the head (atomicMax on the bit pattern of a non-negative float).
+// ---------------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) vmeans_kernel(const uint16_t* __restrict__ v, const int32_t* __restrict__ perm,
+                                                     int S, int demean, uint16_t* __restrict__ mub,
+                                                     unsigned int* __restrict__ amax_bits) {
+  constexpr int SPLIT = 256 / D;  // threads per column
+  const int j = blockIdx.x, bh = blockIdx.y;
+  const int nkb = (S + 127) / 128;
+  const int d = threadIdx.x % D, part = threadIdx.x / D;
+  const int t0 = j * 128, n = min(128, S - t0);
+  const uint16_t* vh = v + (int64_t)bh * S * D;
+  const int32_t* ph = perm ? perm + (int64_t)bh * S : nullptr;
+  __shared__ double sums[SPLIT][D];
+  __shared__ float mus[D];
+  __shared__ float red[8];
+  double s = 0.0;
+  for (int r = part; r < n; r += SPLIT) {
+    int src = ph ? ph[t0 + r] : t0 + r;
+    s += (double)bf16_bits_to_f32(vh[(int64_t)src * D + d]);
+  }
+  sums[part][d] = s;
+  __syncthreads();
+  if (part == 0) {
+    double tot = 0.0;
+#pragma unroll
+    for (int q = 0; q < SPLIT; ++q) tot += sums[q][d];
+    uint16_t b = demean ? f64_to_bf16_rne(tot / (double)n) : (uint16_t)0;
+    mub[((int64_t)bh * nkb + j) * D + d] = b;
+    mus[d] = bf16_bits_to_f32(b);
+  }
+  __syncthreads();
+  float amax = 0.f;
+  for (int r = part; r < n; r += SPLIT) {
+    int src = ph ? ph[t0 + r] : t0 + r;
+    float res = __fsub_rn(bf16_bits_to_f32(vh[(int64_t)src * D + d]), mus[d]);
+    amax = fmaxf(amax, fabsf(res));
+  }
+  for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float m = red[0];
+    for (int w = 1; w < 8; ++w) m = fmaxf(m, red[w]);
+    atomicMax(amax_bits + bh, __float_as_uint(m));
+  }
+}
+
+// Residual codes, transposed: Vt[bh][d][t] = E4M3(R[t][d] * 448/amax_h), t < S_pad (pad = 0).
+// One CTA per (block, bh); the 128 x D code tile is transposed through shared memory so that
+// each d-row of 128 codes is written with one coalesced 128-byte store.
+template <int D>
+__global__ void __launch_bounds__(256) vpack_kernel(const uint16_t* __restrict__ v, const int32_t* __restrict__ perm,
+                                                    int S, int S_pad, const uint16_t* __restrict__ mub,
+                                                    const unsigned int* __restrict__ amax_bits,
+                                                    uint8_t* __restrict__ vt, float* __restrict__ sv) {
+  const int j = blockIdx.x, bh = blockIdx.y;
+  const int nkb = S_pad / 128;
+  const uint16_t* vh = v + (int64_t)bh * S * D;
+  const int32_t* ph = perm ? perm + (int64_t)bh * S : nullptr;
+  __shared__ uint8_t tile[D][128 + 16];
+  const float amax = __uint_as_float(amax_bits[bh]);
+  const bool zero = !(amax > 0.f);
+  const float inv = zero ? 1.f : __fdiv_rn(448.f, amax);
+  if (j == 0 && threadIdx.x == 0) sv[bh] = zero ? 1.f : __fdiv_rn(amax, 448.f);
+  const uint16_t* mu = mub + ((int64_t)bh * nkb + j) * D;
+  // each thread converts 8 consecutive channels of one row (one 16-byte load)
+  constexpr int CPR = D / 8;
+  for (int c = threadIdx.x; c < 128 * CPR; c += 256) {
+    int r = c / CPR, cc = c % CPR;
+    int t = j * 128 + r;
+    uint32_t codes2[4] = {0, 0, 0, 0};
+    if (t < S) {
+      int src = ph ? ph[t] : t;
+      uint4 raw = *reinterpret_cast<const uint4*>(vh + (int64_t)src * D + cc * 8);
+      uint4 mraw = *reinterpret_cast<const uint4*>(mu + cc * 8);
+      const uint32_t* w = reinterpret_cast<const uint32_t*>(&raw);
+      const uint32_t* mw = reinterpret_cast<const uint32_t*>(&mraw);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float r0 = __fsub_rn(bf16_bits_to_f32(w[q] & 0xFFFFu), bf16_bits_to_f32(mw[q] & 0xFFFFu));
+        float r1 = __fsub_rn(bf16_bits_to_f32(w[q] >> 16), bf16_bits_to_f32(mw[q] >> 16));
+        codes2[q] = cvt_e4m3x2(__fmul_rn(r0, inv), __fmul_rn(r1, inv));
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      tile[cc * 8 + 2 * q][r] = (uint8_t)(codes2[q] & 0xFF);
+      tile[cc * 8 + 2 * q + 1][r] = (uint8_t)(codes2[q] >> 8);
+    }
+  }
+  __syncthreads();
+  // write D rows of 128 bytes: 8 threads per row, 16 bytes each
+  uint8_t* out = vt + (int64_t)bh * D * S_pad + (int64_t)j * 128;
+  for (int c = threadIdx.x; c < D * 8; c += 256) {
+    int d = c / 8, seg = c % 8;
+    uint4 val = *reinterpret_cast<const uint4*>(&tile[d][seg * 16]);
+    *reinterpret_cast<uint4*>(out + (int64_t)d * S_pad + seg * 16) = val;
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Host-side launch sequence of the prepare step (all on one stream, no host synchronisation).
+// ---------------------------------------------------------------------------------------------
+static int check_launch() { return cudaPeekAtLastError() == cudaSuccess ? 0 : VC_ERR_CUDA; }
+
+int prepare_launch(const PlanBuffers& p, const uint16_t* Q, const uint16_t* K, const uint16_t* V,
+                   const int32_t* perm_in, bool vsmooth, int iters, cudaStream_t st) {
+  const int BH = p.B * p.H, S = p.S, D = p.D, k = p.k, nkb = p.nkb, S_pad = p.S_pad;
+  dim3 gblk(nkb, BH);
+  // Q: per-block quantisation in token order
+  if (D == 128) quant_blocks_kernel<128><<<gblk, 256, 0, st>>>(Q, nullptr, S, S_pad, p.qcodes, p.qscales);
+  else quant_blocks_kernel<64><<<gblk, 256, 0, st>>>(Q, nullptr, S, S_pad, p.qcodes, p.qscales);
+  if (check_launch()) return VC_ERR_CUDA;
+  const int32_t* perm = nullptr;
+  if (vsmooth) {
+    if (perm_in) {
+      if (cudaMemcpyAsync(p.perm, perm_in, sizeof(int32_t) * (size_t)BH * S, cudaMemcpyDeviceToDevice, st) !=
+          cudaSuccess)
+        return VC_ERR_CUDA;
+    } else {
+      static bool attr_set = false;
+      if (!attr_set) {
+        if (cudaFuncSetAttribute(kmeans_assign_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kmeans_assign_smem<128>()) != cudaSuccess ||
+            cudaFuncSetAttribute(kmeans_assign_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kmeans_assign_smem<64>()) != cudaSuccess)
+          return VC_ERR_CUDA;
+        attr_set = true;
+      }
+      kmeans_init_kernel<<<dim3(k, BH), 128, 0, st>>>(V, S, D, k, p.cent, p.cnorm);
+      for (int it = 0; it < iters; ++it) {
+        dim3 ga((S + 63) / 64, BH);
+        if (D == 128)
+          kmeans_assign_kernel<128><<<ga, 256, kmeans_assign_smem<128>(), st>>>(V, S, k, p.cent, p.cnorm, p.labels);
+        else
+          kmeans_assign_kernel<64><<<ga, 256, kmeans_assign_smem<64>(), st>>>(V, S, k, p.cent, p.cnorm, p.labels);
+        argsort_kernel<<<BH, 1024, 0, st>>>(p.labels, S, k, p.perm, p.counts, p.offsets);
+        kmeans_update_kernel<<<dim3(k, BH), 128, 0, st>>>(V, S, D, k, p.perm, p.counts, p.offsets, p.cent, p.cnorm);
+      }
+    }
+    perm = p.perm;
+  } else {
+    int64_t total = (int64_t)BH * S;
+    iota_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(p.perm, S, total);
+  }
+  if (check_launch()) return VC_ERR_CUDA;
+  // K' = K[pi], per-block quantisation
+  if (D == 128) quant_blocks_kernel<128><<<gblk, 256, 0, st>>>(K, perm, S, S_pad, p.kcodes, p.kscales);
+  else quant_blocks_kernel<64><<<gblk, 256, 0, st>>>(K, perm, S, S_pad, p.kcodes, p.kscales);
+  // V' = V[pi]: block means, residual maximum per head, residual codes transposed
+  if (cudaMemsetAsync(p.vamax, 0, sizeof(unsigned int) * BH, st) != cudaSuccess) return VC_ERR_CUDA;
+  if (D == 128) {
+    vmeans_kernel<128><<<gblk, 256, 0, st>>>(V, perm, S, vsmooth ? 1 : 0, p.means, p.vamax);
+    vpack_kernel<128><<<gblk, 256, 0, st>>>(V, perm, S, S_pad, p.means, p.vamax, p.vcodes, p.vscales);
+  } else {
+    vmeans_kernel<64><<<gblk, 256, 0, st>>>(V, perm, S, vsmooth ? 1 : 0, p.means, p.vamax);
+    vpack_kernel<64><<<gblk, 256, 0, st>>>(V, perm, S, S_pad, p.means, p.vamax, p.vcodes, p.vscales);
+  }
+  return check_launch();
+}
+
+}  // namespace vc

@@ -1,0 +1,155 @@
+/*
+ * vc_attn.h -- C ABI of the GB300 (sm_103a) ExpCast-FP8 + V-Smooth FP8 attention forward.
+ *
+ * The operation is the non-causal self-attention forward of
+ *   "VC-Attention: Value Smoothing and Softmax Casting for Low-bit Attention"
+ *   (Sec. 3.1 Eq. 1 online softmax; Sec. 3.2 Eq. 3-6 value-guided permutation, block demeaning
+ *   and online mean restoration; Sec. 3.3 Eq. 7 ExpCast-FP8)
+ * with the scheduling rules of
+ *   "Open-VC Attention: an open-source, error-tunable variant of VC-Attention" (MachGen blog),
+ *   "Scheduling around ExpCast": Q/K scaled per 128-token block, V per head, one FMA per score,
+ *   running maximum on the true score with every increase applied, row sum built from the
+ *   decoded FP8 probabilities that feed PV, mid-window key order, packed transposed V.
+ *
+ * Conventions shared by every call:
+ *   - Pointers named as device pointers must be device memory on the current CUDA device
+ *     (or managed memory); host pointers are plain host memory.
+ *   - Tensors are dense, row-major, without padding: Q, K, V, O are bf16 [B, H, S, D].
+ *   - All work is enqueued on `stream` (0 = legacy default stream) and is asynchronous: inputs
+ *     must stay valid and unmodified until the stream reaches the call; outputs are ready when
+ *     the stream has passed it.
+ *   - Return value: VC_OK (0) or a negative VC_ERR_* code. Nothing aborts or prints. On an
+ *     error the outputs are unspecified and the plan (if any) is left usable or destroyed as
+ *     stated per call.
+ *   - Supported shapes: D in {64, 128}; 1 <= S <= 1048576; B*H >= 1; B*H*ceil(S/128)*128*D below
+ *     2^40 bytes; 1 <= k_clusters <= min(S, 1024); 0 <= iters <= 64.
+ *   - No CPU fallback: every step of the computation runs in this library's CUDA kernels.
+ */
+#ifndef VC_ATTN_H
+#define VC_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------------------------- */
+enum {
+  VC_OK = 0,
+  VC_ERR_INVALID_ARG = -1,   /* null pointer, bad size or flag combination                */
+  VC_ERR_UNSUPPORTED = -2,   /* shape outside the supported set (e.g. D not 64/128)       */
+  VC_ERR_CUDA = -3,          /* a CUDA runtime call or kernel launch failed               */
+  VC_ERR_TIMEOUT = -4,       /* a kernel gave up waiting on an internal hand-off          */
+  VC_ERR_PLAN_MISMATCH = -5, /* an existing plan has a different shape                    */
+  VC_ERR_OOM = -6,           /* device allocation failed                                  */
+  VC_ERR_NO_DEVICE = -7      /* the current device is not an sm_103 GPU                   */
+};
+
+/* ---- flags ----------------------------------------------------------------------------- */
+enum {
+  /* Score -> E4M3 probability code by one FMA, Eq. 7 of the VC-Attention paper (Sec. 3.3).
+     Off: exponentiate in fp32 (exp2f) and convert with a rounding E4M3 cast. */
+  VC_EXPCAST = 1u,
+  /* V-Smooth (Sec. 3.2): k-means grouping, permutation of K and V, 128-row block means
+     restored in the accumulator. Off (prepare): identity permutation and no means. */
+  VC_VSMOOTH = 2u,
+  /* Mid-window key order ("Open-VC Attention", mid-window key traversal): query tile qt starts
+     at key tile min(nkb-1, qt+2), sweeps down to tile 0, then visits the tail. Off: 0..nkb-1. */
+  VC_MIDWINDOW = 4u,
+  /* Test hook: the forward kernel's first internal wait gives up at once, so the call reports
+     VC_ERR_TIMEOUT through vc_plan_status() without hanging. */
+  VC_DEBUG_TIMEOUT = 1u << 16
+};
+#define VC_FLAGS_DEFAULT (VC_EXPCAST | VC_VSMOOTH | VC_MIDWINDOW)
+
+/* ---- the plan ----------------------------------------------------------------------------
+ * Opaque object owning the device buffers the prepare step writes and the forward reads:
+ * the permutation pi, the E4M3 codes of Q and of K' = K[pi] with one fp32 scale per 128-token
+ * block, the E4M3 codes of the V' residual stored transposed and zero-padded as [B, H, D, S_pad]
+ * (key dimension contiguous, the layout of the PV operand) with one fp32 scale per head, the
+ * bf16 128-row block means, the k-means labels and centroids, and a device status word.
+ * S_pad = 128 * ceil(S/128).  The library owns these buffers until vc_plan_destroy().        */
+typedef struct vc_plan vc_plan;
+
+/* vc_attn_prepare
+ * Grouping and quantisation (VC-Attention Sec. 3.2 "Value-guided permutation", "Block
+ * demeaning"; Sec. 3.4 "Fused preprocessing"; Open-VC "Fused input preparation"):
+ *   per (b, h): k-means over the V rows (k_clusters centroids, `iters` Lloyd rounds, started
+ *   from the rows floor(i*S/k)), pi = stable argsort of the labels, K' = K[pi], V' = V[pi];
+ *   Q and K' quantised to E4M3 with one scale per 128-token block (scale = absmax/448);
+ *   mu_j = mean of the valid rows of block j of V', stored as bf16; R = V' - mu_j quantised to
+ *   E4M3 with one scale per head (absmax/448), stored transposed and padded.
+ * Q, K, V: device bf16 [B, H, S, D].  k_clusters, iters: k-means size and rounds (iters = 0
+ * keeps the initial assignment of the first round).  *plan: NULL to allocate a new plan, or an
+ * existing plan of the same (B, H, S, D, k_clusters), whose buffers are reused without any
+ * allocation (VC_ERR_PLAN_MISMATCH if the shape differs; the plan is left untouched).
+ * The first call allocates device memory (synchronous cudaMalloc); later calls reusing the plan
+ * are fully asynchronous and can be captured in a CUDA graph. */
+int vc_attn_prepare(const void* Q, const void* K, const void* V, int B, int H, int S, int D, int k_clusters,
+                    int iters, cudaStream_t stream, vc_plan** plan);
+
+/* vc_attn_prepare_ex -- vc_attn_prepare with control over grouping.
+ * perm: NULL, or a device int32 [B, H, S] permutation per (b, h) to use instead of k-means
+ *   (reusing the permutation across denoising steps, VC-Attention Sec. 3.4 "Amortized grouping
+ *   schedule"; it is not checked to be a permutation -- every entry must lie in [0, S)).
+ * flags: VC_VSMOOTH set -> group (unless perm is given) and demean; clear -> identity
+ *   permutation (perm ignored), no means, R = V.  Other bits are ignored here. */
+int vc_attn_prepare_ex(const void* Q, const void* K, const void* V, int B, int H, int S, int D, int k_clusters,
+                       int iters, const int32_t* perm, unsigned flags, cudaStream_t stream, vc_plan** plan);
+
+/* vc_attn_forward
+ * The fused attention forward (VC-Attention Eq. 1, 6, 7): for every query row, key tiles of
+ * 128 are visited in the chosen order; S = Q K'^T on FP8 tensor cores; the running maximum is
+ * kept on the true score in code units and every increase rescales the accumulator; each score
+ * becomes an E4M3 code c = clip[0,120](rne(S*a_j + 119.65 - M)) with a_j = 8 log2(e)/sqrt(D)
+ * * sQ * sK_j (or the exp-then-cast path without VC_EXPCAST); the codes multiply the residual
+ * codes of V' on FP8 tensor cores; the row sum of the decoded codes (the denominator) and the
+ * block means (VC_VSMOOTH) enter the accumulator; O = sV * A / l in bf16.
+ * plan: from vc_attn_prepare.  O: device bf16 [B, H, S, D], rows in the original token order.
+ * flags: VC_EXPCAST | VC_MIDWINDOW | VC_VSMOOTH (VC_VSMOOTH is ignored when the plan was
+ * prepared without means) | VC_DEBUG_TIMEOUT.  Kernel-side timeouts are reported
+ * asynchronously through vc_plan_status(). Allocates nothing; can be captured in a graph. */
+int vc_attn_forward(const vc_plan* plan, void* O, unsigned flags, cudaStream_t stream);
+
+/* ---- plan inspection (tests, benchmarks, reuse of pi) ----------------------------------- */
+enum {
+  VC_PLAN_LABELS = 1,    /* int32 [B, H, S]       k-means labels of the last round            */
+  VC_PLAN_PERM = 2,      /* int32 [B, H, S]       pi                                          */
+  VC_PLAN_QCODES = 3,    /* uint8 [B, H, S_pad, D] E4M3 codes of Q (pad rows 0)              */
+  VC_PLAN_QSCALES = 4,   /* fp32  [B, H, nkb]                                                 */
+  VC_PLAN_KCODES = 5,    /* uint8 [B, H, S_pad, D] E4M3 codes of K' = K[pi]                  */
+  VC_PLAN_KSCALES = 6,   /* fp32  [B, H, nkb]                                                 */
+  VC_PLAN_VCODES = 7,    /* uint8 [B, H, D, S_pad] E4M3 codes of the residual, transposed     */
+  VC_PLAN_VSCALES = 8,   /* fp32  [B, H]           per-head residual scale                    */
+  VC_PLAN_MEANS = 9,     /* bf16  [B, H, nkb, D]   block means of V'                          */
+  VC_PLAN_CENTROIDS = 10 /* fp32  [B, H, k, D]     centroids after the last update           */
+};
+/* Size in bytes of one plan tensor (0 for an unknown `what` or a NULL plan). */
+size_t vc_plan_size(const vc_plan* plan, int what);
+/* Enqueue a copy of one plan tensor into dst (host or device memory, `bytes` >= its size). */
+int vc_plan_get(const vc_plan* plan, int what, void* dst, size_t bytes, cudaStream_t stream);
+/* Synchronise `stream`, read and clear the plan's device status word. Returns VC_OK, or
+ * VC_ERR_TIMEOUT if a kernel recorded a timeout since the last call (bits in *bits if non-NULL). */
+int vc_plan_status(vc_plan* plan, cudaStream_t stream, int* bits);
+/* Shape of a plan; any output pointer may be NULL. */
+int vc_plan_shape(const vc_plan* plan, int* B, int* H, int* S, int* D, int* k_clusters);
+/* Free a plan and its device buffers (synchronises the device first). NULL is a no-op. */
+void vc_plan_destroy(vc_plan* plan);
+
+/* ---- single-step exports (unit tests of individual steps) ------------------------------ */
+/* ExpCast-FP8 codes (VC-Attention Eq. 7): out[i] = clip[0,120](rne(fmaf(s[i], a[i], b[i]))),
+ * computed by the forward kernel's own code path.  s, a, b: device fp32 [n]; out: device u8. */
+int vc_expcast_encode(const float* s, const float* a, const float* b, int64_t n, uint8_t* out, cudaStream_t stream);
+
+/* Human-readable text of a status code (static storage). */
+const char* vc_strerror(int status);
+/* Library version string. */
+const char* vc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* VC_ATTN_H */

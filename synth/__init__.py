@@ -109,7 +109,8 @@ def make_inputs(cfg: dict, seed: int = 0, device="cpu"):
             ib = torch.from_numpy(rng.integers(0, S, size=4096)).to(dev)
             sig = float(((q[ia] * k[ib]).sum(dim=1) / math.sqrt(D)).std().item())
             target = 0.5 if h in uniform else 3.0
-            f = math.sqrt(target / max(sig, 1e-12))
+            # a one-token sequence has no score spread to normalise: leave the projections as drawn
+            f = math.sqrt(target / sig) if sig > 1e-6 else 1.0
             q = q * f
             k = k * f
             n_out = int(round(cfg["outlier_frac"] * S))

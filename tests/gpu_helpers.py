@@ -1,0 +1,86 @@
+"""Shared helpers for the GPU parity tests: run the CUDA path through the C ABI, run the CPU
+oracle on the same inputs, and compare with the acceptance rule of the forward.
+
+Acceptance (per batch-head, over the compared rows): relative L2 error <= 1e-2 and max-abs error
+<= 3e-2 * max|V|, with the oracle fed the GPU's permutation. ExpCast codes, the argsort
+permutation and (expected) every prepare output are compared bit for bit.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+REL_L2 = 1e-2
+MAX_ABS_FRAC = 3e-2
+
+
+def u16(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def vc():
+    from bit_fp8_attention_gb300 import build
+
+    build.build()
+    import bit_fp8_attention_gb300 as mod
+
+    return mod
+
+
+def plan_host(m, plan, what) -> np.ndarray:
+    t = m.vc_plan_get(plan, what)
+    torch.cuda.synchronize()
+    if t.dtype == torch.bfloat16:
+        return u16(t)
+    return t.cpu().numpy()
+
+
+def gpu_plan_head(m, plan, b, h) -> dict:
+    """The GPU's prepare outputs for one batch-head, in the oracle's layouts."""
+    g = {}
+    g["perm"] = plan_host(m, plan, m.VC_PLAN_PERM)[b, h]
+    g["labels"] = plan_host(m, plan, m.VC_PLAN_LABELS)[b, h]
+    g["qc"] = plan_host(m, plan, m.VC_PLAN_QCODES)[b, h]
+    g["sq"] = plan_host(m, plan, m.VC_PLAN_QSCALES)[b, h]
+    g["kc"] = plan_host(m, plan, m.VC_PLAN_KCODES)[b, h]
+    g["sk"] = plan_host(m, plan, m.VC_PLAN_KSCALES)[b, h]
+    g["rc"] = np.ascontiguousarray(plan_host(m, plan, m.VC_PLAN_VCODES)[b, h].T)  # [S_pad, D]
+    g["sv"] = float(plan_host(m, plan, m.VC_PLAN_VSCALES)[b, h])
+    g["mub"] = plan_host(m, plan, m.VC_PLAN_MEANS)[b, h]
+    return g
+
+
+def compare_prep(g: dict, o: dict, S: int):
+    """Bit-exact comparison of the GPU and oracle prepare outputs of one head."""
+    assert np.array_equal(g["qc"], o["qc"]), "Q codes differ"
+    assert np.array_equal(g["sq"], o["sq"]), "Q scales differ"
+    assert np.array_equal(g["kc"], o["kc"]), "K' codes differ"
+    assert np.array_equal(g["sk"], o["sk"]), "K' scales differ"
+    assert np.array_equal(g["mub"], o["mub"]), "block means differ"
+    assert g["sv"] == np.float32(o["sv"]), "V scale differs"
+    assert np.array_equal(g["rc"], o["rc"]), "residual codes differ"
+
+
+def errors(gpu_rows: np.ndarray, ref_rows: np.ndarray) -> tuple[float, float]:
+    d = gpu_rows - ref_rows
+    return float(np.linalg.norm(d) / max(np.linalg.norm(ref_rows), 1e-300)), float(np.abs(d).max())
+
+
+def assert_within(gpu_rows, ref_rows, vmax, what=""):
+    rel, mx = errors(gpu_rows, ref_rows)
+    assert rel <= REL_L2, f"{what} rel-L2 {rel:.3e} > {REL_L2}"
+    assert mx <= MAX_ABS_FRAC * vmax, f"{what} max-abs {mx:.3e} > {MAX_ABS_FRAC} * {vmax:.3e}"
+    return rel, mx
+
+
+def oracle_forward_from_plan(g: dict, S: int, rows, expcast=True, midwindow=True, with_mean=True):
+    """Oracle (i) on the GPU's own plan tensors: isolates the forward kernel."""
+    return oracle.attention_quant(g["qc"], g["sq"], g["kc"], g["sk"], g["rc"], g["sv"],
+                                  g["mub"] if with_mean else None, S, rows,
+                                  (oracle.EXPCAST if expcast else 0) | (oracle.MIDWINDOW if midwindow else 0))[0]

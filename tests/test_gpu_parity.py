@@ -1,0 +1,158 @@
+"""GPU parity through the C ABI against the CPU oracle on seeded synthetic inputs.
+
+The forward follows "VC-Attention: Value Smoothing and Softmax Casting for Low-bit Attention"
+(Eq. 1, 3-7) and "Open-VC Attention" ("Scheduling around ExpCast"). Acceptance: ExpCast codes and
+argsort permutations bit-exact; O within rel-L2 1e-2 and max-abs 3e-2 max|V| per head against the
+quantised oracle fed the GPU's permutation; the k-means objective within 1% of the oracle's.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_helpers import (assert_within, compare_prep, errors, f64, gpu_plan_head, oracle_forward_from_plan, u16,
+                         vc)
+
+pytestmark = pytest.mark.gpu
+
+# Forward-only comparison (oracle run on the GPU's own codes): the two sides differ only by the
+# tensor core's fp32 accumulation order for S and PV, ex2.approx for the rescale factor, the
+# rank-16 mean update in fp32 and the final bf16 rounding (2^-9 relative), so a much tighter bound
+# than the end-to-end acceptance applies.
+FWD_ONLY_REL = 4e-3
+
+
+@pytest.fixture(scope="module")
+def m():
+    return vc()
+
+
+def test_expcast_encode_bit_exact(m):
+    rng = np.random.default_rng(0)
+    n = 1 << 20
+    M = rng.normal(0, 300, n).astype(np.float32)
+    a = rng.uniform(1e-3, 2.0, n).astype(np.float32)
+    s = (M / a + rng.normal(0, 40, n)).astype(np.float32)
+    b = (np.float32(119.65) - M).astype(np.float32)
+    s[:8] = [0, -0.0, 1e30, -1e30, 3.4e38, -3.4e38, 1e-40, -1e-40]
+    want = oracle.expcast_codes(s, a, b)
+    got = m.vc_expcast_encode(*(torch.from_numpy(x).cuda() for x in (s, a, b))).cpu().numpy()
+    assert np.array_equal(got, want)
+    assert (want == 120).any() and (want == 0).any() and ((want > 0) & (want < 120)).mean() > 0.3
+
+
+def run(m, cfg, seed=0, vsmooth=True, perm=None):
+    Q, K, V = synth.make_inputs(cfg, seed=seed, device="cuda")
+    plan = m.vc_attn_prepare_ex(Q, K, V, cfg["k"], cfg["iters"], perm=perm, flags=m.VC_VSMOOTH if vsmooth else 0)
+    torch.cuda.synchronize()
+    return Q, K, V, plan
+
+
+def check_config(m, cfg, rows_per_head=None, kmeans_heads=None, seed=0):
+    Q, K, V, plan = run(m, cfg, seed)
+    O = m.vc_attn_forward(plan)
+    torch.cuda.synchronize()
+    assert m.vc_plan_status(plan)[0] == 0
+    S = cfg["S"]
+    rng = np.random.default_rng(seed + 1)
+    for b in range(cfg["B"]):
+        for h in range(cfg["H"]):
+            g = gpu_plan_head(m, plan, b, h)
+            qh, kh, vh = u16(Q[b, h]), u16(K[b, h]), u16(V[b, h])
+            # argsort: bit-exact given the GPU's labels
+            assert np.array_equal(g["perm"], oracle.stable_argsort(g["labels"], cfg["k"]))
+            if kmeans_heads is None or h in kmeans_heads:
+                _, _, J = oracle.kmeans(vh, cfg["k"], cfg["iters"])
+                Jg = oracle.kmeans_objective(vh, cfg["k"], g["labels"])
+                assert abs(Jg - J[-1]) <= 0.01 * J[-1], f"head {h}: J_gpu {Jg} vs J_oracle {J[-1]}"
+            o = oracle.prepare_head(qh, kh, vh, cfg["k"], cfg["iters"], perm=g["perm"])
+            compare_prep(g, o, S)
+            if rows_per_head is None:
+                rows = np.arange(S)
+            else:
+                tiles = rng.choice((S + 127) // 128, size=min(2, (S + 127) // 128), replace=False)
+                rows = np.unique(np.concatenate([np.arange(t * 128, min(S, t * 128 + 128)) for t in tiles] +
+                                                [rng.choice(S, rows_per_head, replace=False), [0, S - 1]]))
+            ref, _, _ = oracle.forward_head(o, rows)
+            got = f64(O[b, h])[rows]
+            vmax = float(np.abs(f64(V[b, h])).max())
+            assert_within(got, ref, vmax, f"head {h}")
+            rel_f, _ = errors(got, oracle_forward_from_plan(g, S, rows))
+            assert rel_f <= FWD_ONLY_REL, f"head {h}: forward-only rel-L2 {rel_f:.3e}"
+    plan.destroy()
+
+
+def test_tiny_config_all_rows(m):
+    check_config(m, synth.config("tiny"))
+
+
+def test_small_config_sampled_rows(m):
+    check_config(m, synth.config("small"), rows_per_head=64, kmeans_heads={0, 5})
+
+
+@pytest.mark.parametrize("S,D", [(1, 128), (127, 128), (129, 64), (255, 128), (300, 64), (1000, 128), (2049, 64)])
+def test_ragged_shapes(m, S, D):
+    cfg = synth.custom(S, D=D, H=2, k=max(1, min(S, S // 100 + 1)), iters=2)
+    check_config(m, cfg)
+
+
+@pytest.mark.parametrize("expcast,midwindow,vsmooth", [(False, True, True), (True, False, True),
+                                                       (True, True, False), (False, False, False)])
+def test_ablations(m, expcast, midwindow, vsmooth):
+    cfg = synth.custom(700, D=128, H=2, k=6, iters=3, outlier_frac=0.01)
+    Q, K, V, plan = run(m, cfg, seed=3, vsmooth=vsmooth)
+    flags = (m.VC_EXPCAST if expcast else 0) | (m.VC_MIDWINDOW if midwindow else 0) | m.VC_VSMOOTH
+    O = m.vc_attn_forward(plan, flags=flags)
+    torch.cuda.synchronize()
+    for h in range(2):
+        g = gpu_plan_head(m, plan, 0, h)
+        o = oracle.prepare_head(u16(Q[0, h]), u16(K[0, h]), u16(V[0, h]), 6, 3, vsmooth=vsmooth,
+                                perm=g["perm"] if vsmooth else None)
+        compare_prep(g, o, 700)
+        rows = np.arange(700)
+        ref, _, _ = oracle.forward_head(o, rows, expcast=expcast, midwindow=midwindow)
+        assert_within(f64(O[0, h]), ref, float(np.abs(f64(V[0, h])).max()), f"head {h}")
+
+
+def test_explicit_permutation_and_plan_reuse(m):
+    cfg = synth.custom(513, D=128, H=2, k=5, iters=2)
+    Q, K, V = synth.make_inputs(cfg, seed=4, device="cuda")
+    perm = torch.stack([torch.randperm(513, generator=torch.Generator().manual_seed(i)) for i in range(2)])
+    perm = perm.to(torch.int32).reshape(1, 2, 513).cuda().contiguous()
+    plan = m.vc_attn_prepare_ex(Q, K, V, 5, 2, perm=perm)
+    O1 = m.vc_attn_forward(plan).clone()
+    plan2 = m.vc_attn_prepare_ex(Q, K, V, 5, 2, perm=perm, plan=plan)  # reuse: no allocation
+    assert plan2 is plan
+    O2 = m.vc_attn_forward(plan)
+    torch.cuda.synchronize()
+    assert torch.equal(O1, O2)
+    for h in range(2):
+        o = oracle.prepare_head(u16(Q[0, h]), u16(K[0, h]), u16(V[0, h]), 5, 2, perm=perm[0, h].cpu().numpy())
+        ref, _, _ = oracle.forward_head(o, np.arange(513))
+        assert_within(f64(O1[0, h]), ref, float(np.abs(f64(V[0, h])).max()))
+    # a plan of another shape is refused and left intact
+    Q2, K2, V2 = (t[:, :, :256].contiguous() for t in (Q, K, V))
+    with pytest.raises(m.VCError) as e:
+        m.vc_attn_prepare(Q2, K2, V2, 5, 2, plan=plan)
+    assert e.value.rc == m.VC_ERR_PLAN_MISMATCH
+    O3 = m.vc_attn_forward(plan)
+    torch.cuda.synchronize()
+    assert torch.equal(O1, O3)
+    plan.destroy()
+
+
+def test_forced_timeout_reports_status_and_recovers(m):
+    cfg = synth.custom(384, D=128, H=1, k=3, iters=2)
+    Q, K, V, plan = run(m, cfg, seed=5)
+    m.vc_attn_forward(plan, flags=m.VC_FLAGS_DEFAULT | m.VC_DEBUG_TIMEOUT)
+    rc, bits = m.vc_plan_status(plan)
+    assert rc == m.VC_ERR_TIMEOUT and bits != 0
+    O = m.vc_attn_forward(plan)  # the context is still usable and the next call is clean
+    rc, bits = m.vc_plan_status(plan)
+    assert rc == 0 and bits == 0
+    g = gpu_plan_head(m, plan, 0, 0)
+    ref = oracle_forward_from_plan(g, 384, np.arange(384))
+    rel, _ = errors(f64(O[0, 0]), ref)
+    assert rel <= FWD_ONLY_REL
+    plan.destroy()
