@@ -1,0 +1,340 @@
+"""Benchmark of the ExpCast-FP8 + V-Smooth attention hot path on GB300.
+
+A step is one pass of the whole hot path over one batch: vc_attn_prepare (Q/K block quantisation,
+k-means grouping, stable argsort, K/V gather, bf16 block means, residual codes) followed by
+vc_attn_forward. `value` = 4*B*H*S^2*D per step / step time (TFLOP/s, inputs resident in HBM).
+The forward alone (the pages' kernel metric, preprocessing outside the timer) is reported as
+`forward_tflops` and in `roofline`; the prepare time is split into grouping and quantisation and
+amortised over the grouping schedule of the pages (a 40-step run regroups at steps 0, 4, 8).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config wan] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "attention TFLOP/s (4BHS^2D/t) at S=75600,H=40,D=128; % of FP8 dense peak"
+FP8_OVER_BF16 = 4.5 / 2.25  # nominal dense FP8 / BF16 tensor ratio on GB300
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="wan")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload_name(cfg):
+    return (f"{cfg['name']}: B={cfg['B']} H={cfg['H']} S={cfg['S']} D={cfg['D']} "
+            f"grid={'x'.join(map(str, cfg['grid']))} k={cfg['k']} iters={cfg['iters']}")
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except Exception:
+        return 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200", "-f", self.path],
+                                         stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[4:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [r[0] for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2][1:]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+def launches_per_step(cfg) -> int:
+    # prepare: Q quant, k-means init, (assign, argsort, update) x iters, K' quant, means, residual pack
+    return 5 + 3 * cfg["iters"] + 1  # + the fused forward
+
+
+def cpu_baseline(cfg, Q, K, V, budget_rows: int = 48):
+    """The oracle, as it stands, on a bounded sample of the workload, extrapolated to one step."""
+    import oracle
+
+    oracle.build()
+    S, H, D, k = cfg["S"], cfg["H"], cfg["D"], cfg["k"]
+    q, kk, v = (oracle._u16(t[0, 0].cpu()) for t in (Q, K, V))
+    t0 = time.perf_counter()
+    oracle.kmeans(v, k, 1)  # one Lloyd round on one head
+    t_km = (time.perf_counter() - t0) * cfg["iters"] * cfg["B"] * H
+    t0 = time.perf_counter()
+    labels = np.arange(S, dtype=np.int32) * k // S
+    perm = oracle.stable_argsort(labels, k)
+    prep = oracle.prepare_head(q, kk, v, k, cfg["iters"], perm=perm)
+    t_prep = (time.perf_counter() - t0) * cfg["B"] * H
+    rows = np.random.default_rng(0).choice(S, budget_rows, replace=False)
+    t0 = time.perf_counter()
+    oracle.forward_head(prep, rows)
+    t_fwd = (time.perf_counter() - t0) * (S / budget_rows) * cfg["B"] * H
+    t_step = t_km + t_prep + t_fwd
+    return {
+        "value": synth.flops(cfg) / t_step / 1e12,
+        "unit": "TFLOP/s",
+        "cores": oracle.num_threads(),
+        "kind": "oracle",
+        "sample": (f"head 0 only: 1 k-means round (x{cfg['iters']} rounds x {cfg['B'] * H} heads), quantise/"
+                   f"gather/demean (x{cfg['B'] * H} heads), forward on {budget_rows} random query rows "
+                   f"(x{S}/{budget_rows} rows x {cfg['B'] * H} heads); extrapolated step {t_step:.1f} s"),
+        "extrapolated_step_s": t_step,
+    }
+
+
+def run_reference(args, cfg, rank):
+    """Reference arm: the CPU oracle, timed as it stands on the host cores, same metric/config."""
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    Q, K, V = synth.make_inputs(dict(cfg, H=1), seed=0, device="cpu")
+    times = []
+    for i in range(args.warmup + args.steps):
+        base = cpu_baseline(dict(cfg), Q, K, V, budget_rows=16)
+        if i >= args.warmup:
+            times.append(base["extrapolated_step_s"])
+    t = statistics.mean(times)
+    value = synth.flops(cfg) / t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_name(cfg), "sample": "oracle on head 0 of the same generator, extrapolated"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": base["sample"]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    cfg = synth.config(args.config)
+    if args.impl == "reference":
+        run_reference(args, cfg, rank)
+        return
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    from bit_fp8_attention_gb300 import build as _b
+
+    _b.build()
+    import bit_fp8_attention_gb300 as vc
+
+    Q, K, V = synth.make_inputs(cfg, seed=rank, device=dev)
+    stream = torch.cuda.current_stream()
+    flops = synth.flops(cfg)
+    B, H, S, D = cfg["B"], cfg["H"], cfg["S"], cfg["D"]
+    plan = vc.vc_attn_prepare(Q, K, V, cfg["k"], cfg["iters"])
+    O = torch.empty_like(Q)
+
+    def step(ev=None):
+        vc.vc_attn_prepare(Q, K, V, cfg["k"], cfg["iters"], plan=plan)
+        if ev is not None:
+            ev[0].record(stream)
+        vc.vc_attn_forward(plan, O)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    rc, bits = vc.vc_plan_status(plan)
+    if rc != 0:
+        raise RuntimeError(f"kernel status {rc} bits {bits}")
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    fwd_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(fwd_events[i])
+        t_end.record(stream)
+        barrier()
+    ms_total = t_start.elapsed_time(t_end)
+    fwd_ms = [a.elapsed_time(b) for a, b in fwd_events]
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    value = world * flops / (ms_step * 1e-3) / 1e12
+    clocks = clk.summary()
+
+    # Prepare split (untimed for `value`): quantisation/gather/means with the permutation given,
+    # versus the full prepare with k-means and argsort.
+    perm = vc.vc_plan_get(plan, vc.VC_PLAN_PERM)
+
+    def time_it(fn, reps=3):
+        fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    t_prep_full = time_it(lambda: vc.vc_attn_prepare(Q, K, V, cfg["k"], cfg["iters"], plan=plan))
+    t_prep_quant = time_it(lambda: vc.vc_attn_prepare_ex(Q, K, V, cfg["k"], cfg["iters"], perm=perm, plan=plan))
+    t_group = max(t_prep_full - t_prep_quant, 0.0)
+    vc.vc_attn_prepare(Q, K, V, cfg["k"], cfg["iters"], plan=plan)
+    torch.cuda.synchronize()
+
+    # End to end through the public API from pinned host memory, copies inside the timed region.
+    e2e = None
+    if not args.no_e2e:
+        Qh, Kh, Vh = (t.cpu().pin_memory() for t in (Q, K, V))
+        Oh = torch.empty(O.shape, dtype=O.dtype, device="cpu").pin_memory()
+        Qd, Kd, Vd = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+
+        def e2e_step():
+            Qd.copy_(Qh, non_blocking=True)
+            Kd.copy_(Kh, non_blocking=True)
+            Vd.copy_(Vh, non_blocking=True)
+            vc.vc_attn_prepare(Qd, Kd, Vd, cfg["k"], cfg["iters"], plan=plan)
+            vc.vc_attn_forward(plan, O)
+            Oh.copy_(O, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(2, min(args.steps, 5))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        b.record(stream)
+        barrier()
+        e2e_ms = a.elapsed_time(b) / n_e2e
+        nbytes = Q.numel() * Q.element_size()
+        e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": 3 * nbytes, "d2h_bytes_per_step": nbytes}
+        del Qh, Kh, Vh, Oh, Qd, Kd, Vd
+
+    bf16_burst, bf16_sus, src = measured_peaks()
+    fp8_peak = bf16_burst * FP8_OVER_BF16
+    fwd_avg = statistics.mean(fwd_ms)
+    fwd_tflops = flops / (fwd_avg * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp8_e4m3 (fp32 accumulate)", "data": "synthetic",
+        "config": {"workload": workload_name(cfg), "parallelism": "replicas" if world > 1 else "single GPU",
+                   "step": "vc_attn_prepare (k-means grouping + quantisation) + vc_attn_forward",
+                   "l2": f"inputs larger than L2 (Q, K, V {3 * Q.numel() * 2 / 1e9:.2f} GB), no flush"},
+        "forward_ms": fwd_avg, "forward_tflops": fwd_tflops,
+        "pct_fp8_peak": 100.0 * fwd_tflops / fp8_peak,
+        "prepare_ms": t_prep_full, "prepare_quant_ms": t_prep_quant, "grouping_ms": t_group,
+        "amortised_prepare_ms": t_prep_quant + 3.0 / 40.0 * t_group,
+        "roofline": {"bound": "tensor", "kernel": "vc_fwd_kernel<128>", "achieved": fwd_tflops, "peak": fp8_peak,
+                     "unit": "TFLOP/s", "frac": fwd_tflops / fp8_peak, "traffic": None,
+                     "peak_source": f"{src} bf16 burst {bf16_burst:.0f} TFLOP/s x {FP8_OVER_BF16:.0f} (FP8/BF16 nominal)"},
+        "clocks": clocks, "gpu_launches": launches_per_step(cfg) * args.steps,
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, Q, K, V)
+        line["cpu_baseline"].pop("extrapolated_step_s", None)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    plan.destroy()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -41,19 +41,26 @@ def plan_host(m, plan, what) -> np.ndarray:
     return t.cpu().numpy()
 
 
-def gpu_plan_head(m, plan, b, h) -> dict:
-    """The GPU's prepare outputs for one batch-head, in the oracle's layouts."""
-    g = {}
-    g["perm"] = plan_host(m, plan, m.VC_PLAN_PERM)[b, h]
-    g["labels"] = plan_host(m, plan, m.VC_PLAN_LABELS)[b, h]
-    g["qc"] = plan_host(m, plan, m.VC_PLAN_QCODES)[b, h]
-    g["sq"] = plan_host(m, plan, m.VC_PLAN_QSCALES)[b, h]
-    g["kc"] = plan_host(m, plan, m.VC_PLAN_KCODES)[b, h]
-    g["sk"] = plan_host(m, plan, m.VC_PLAN_KSCALES)[b, h]
-    g["rc"] = np.ascontiguousarray(plan_host(m, plan, m.VC_PLAN_VCODES)[b, h].T)  # [S_pad, D]
-    g["sv"] = float(plan_host(m, plan, m.VC_PLAN_VSCALES)[b, h])
-    g["mub"] = plan_host(m, plan, m.VC_PLAN_MEANS)[b, h]
+def gpu_plan_all(m, plan) -> dict:
+    """Every prepare output of a plan copied to the host once."""
+    return {"perm": plan_host(m, plan, m.VC_PLAN_PERM), "labels": plan_host(m, plan, m.VC_PLAN_LABELS),
+            "qc": plan_host(m, plan, m.VC_PLAN_QCODES), "sq": plan_host(m, plan, m.VC_PLAN_QSCALES),
+            "kc": plan_host(m, plan, m.VC_PLAN_KCODES), "sk": plan_host(m, plan, m.VC_PLAN_KSCALES),
+            "vt": plan_host(m, plan, m.VC_PLAN_VCODES), "sv": plan_host(m, plan, m.VC_PLAN_VSCALES),
+            "mub": plan_host(m, plan, m.VC_PLAN_MEANS)}
+
+
+def head_of(a: dict, b: int, h: int) -> dict:
+    """One batch-head of gpu_plan_all(), in the oracle's layouts (residual codes [S_pad, D])."""
+    g = {key: a[key][b, h] for key in ("perm", "labels", "qc", "sq", "kc", "sk", "mub")}
+    g["rc"] = np.ascontiguousarray(a["vt"][b, h].T)
+    g["sv"] = float(a["sv"][b, h])
     return g
+
+
+def gpu_plan_head(m, plan, b, h) -> dict:
+    """The GPU's prepare outputs for one batch-head (copies the whole plan: small plans only)."""
+    return head_of(gpu_plan_all(m, plan), b, h)
 
 
 def compare_prep(g: dict, o: dict, S: int):

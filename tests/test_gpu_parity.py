@@ -11,8 +11,8 @@ import torch
 
 import oracle
 import synth
-from gpu_helpers import (assert_within, compare_prep, errors, f64, gpu_plan_head, oracle_forward_from_plan, u16,
-                         vc)
+from gpu_helpers import (assert_within, compare_prep, errors, f64, gpu_plan_all, gpu_plan_head, head_of,
+                         oracle_forward_from_plan, u16, vc)
 
 pytestmark = pytest.mark.gpu
 
@@ -56,9 +56,10 @@ def check_config(m, cfg, rows_per_head=None, kmeans_heads=None, seed=0):
     assert m.vc_plan_status(plan)[0] == 0
     S = cfg["S"]
     rng = np.random.default_rng(seed + 1)
+    allp = gpu_plan_all(m, plan)
     for b in range(cfg["B"]):
         for h in range(cfg["H"]):
-            g = gpu_plan_head(m, plan, b, h)
+            g = head_of(allp, b, h)
             qh, kh, vh = u16(Q[b, h]), u16(K[b, h]), u16(V[b, h])
             # argsort: bit-exact given the GPU's labels
             assert np.array_equal(g["perm"], oracle.stable_argsort(g["labels"], cfg["k"]))
@@ -105,8 +106,9 @@ def test_ablations(m, expcast, midwindow, vsmooth):
     flags = (m.VC_EXPCAST if expcast else 0) | (m.VC_MIDWINDOW if midwindow else 0) | m.VC_VSMOOTH
     O = m.vc_attn_forward(plan, flags=flags)
     torch.cuda.synchronize()
+    allp = gpu_plan_all(m, plan)
     for h in range(2):
-        g = gpu_plan_head(m, plan, 0, h)
+        g = head_of(allp, 0, h)
         o = oracle.prepare_head(u16(Q[0, h]), u16(K[0, h]), u16(V[0, h]), 6, 3, vsmooth=vsmooth,
                                 perm=g["perm"] if vsmooth else None)
         compare_prep(g, o, 700)
