@@ -54,6 +54,7 @@ int plan_create(int B, int H, int S, int D, int k, vc_plan** out) {
   b.B = B; b.H = H; b.S = S; b.D = D; b.k = k;
   b.nkb = (S + 127) / 128;
   b.S_pad = b.nkb * 128;
+  b.nkb16 = (b.nkb + 15) / 16 * 16;
   const size_t BH = (size_t)B * H;
   const size_t codes = BH * b.S_pad * D;
   const size_t sizes[] = {
@@ -64,6 +65,7 @@ int plan_create(int B, int H, int S, int D, int k, vc_plan** out) {
       codes,                          // vcodes
       BH * 4,                         // vscales
       BH * b.nkb * D * 2,             // means
+      BH * b.nkb16 * D * 2,           // meansT
       BH * S * 4,                     // labels
       BH * S * 4,                     // perm
       BH * k * D * 4,                 // cent
@@ -83,7 +85,7 @@ int plan_create(int B, int H, int S, int D, int k, vc_plan** out) {
   }
   uint8_t* p = (uint8_t*)blk;
   void** slots[] = {(void**)&b.qcodes, (void**)&b.qscales, (void**)&b.kcodes, (void**)&b.kscales,
-                    (void**)&b.vcodes, (void**)&b.vscales, (void**)&b.means,   (void**)&b.labels,
+                    (void**)&b.vcodes, (void**)&b.vscales, (void**)&b.means,   (void**)&b.meansT, (void**)&b.labels,
                     (void**)&b.perm,   (void**)&b.cent,    (void**)&b.cnorm,   (void**)&b.counts,
                     (void**)&b.offsets, (void**)&b.vamax,  (void**)&b.status};
   for (size_t i = 0; i < sizeof(sizes) / sizeof(sizes[0]); ++i) {

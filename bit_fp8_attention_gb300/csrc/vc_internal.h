@@ -11,6 +11,7 @@ namespace vc {
 // Device buffers of a plan (layouts as documented in vc_attn.h).
 struct PlanBuffers {
   int B, H, S, D, k, nkb, S_pad;
+  int nkb16;            // nkb rounded up to a multiple of 16
   uint8_t* qcodes;      // [BH, S_pad, D]
   float* qscales;       // [BH, nkb]
   uint8_t* kcodes;      // [BH, S_pad, D]
@@ -18,6 +19,7 @@ struct PlanBuffers {
   uint8_t* vcodes;      // [BH, D, S_pad]
   float* vscales;       // [BH]
   uint16_t* means;      // [BH, nkb, D] bf16
+  uint16_t* meansT;     // [BH, D, nkb16] bf16, the same means transposed (pad columns 0)
   int32_t* labels;      // [BH, S]
   int32_t* perm;        // [BH, S]
   float* cent;          // [BH, k, D]
@@ -33,7 +35,7 @@ int prepare_launch(const PlanBuffers& p, const uint16_t* Q, const uint16_t* K, c
                    const int32_t* perm_in, bool vsmooth, int iters, cudaStream_t st);
 
 struct FwdMaps {
-  CUtensorMap q, k, v;
+  CUtensorMap q, k, v, mu;
 };
 int encode_fwd_maps(const PlanBuffers& p, FwdMaps* maps);
 int forward_launch(const PlanBuffers& p, const FwdMaps& maps, uint16_t* O, unsigned flags, cudaStream_t st);

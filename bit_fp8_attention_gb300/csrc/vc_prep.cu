@@ -326,7 +326,8 @@ __global__ void iota_kernel(int32_t* __restrict__ perm, int S, int64_t total) {
 template <int D>
 __global__ void __launch_bounds__(256) vmeans_kernel(const uint16_t* __restrict__ v, const int32_t* __restrict__ perm,
                                                      int S, int demean, uint16_t* __restrict__ mub,
-                                                     unsigned int* __restrict__ amax_bits) {
+                                                     unsigned int* __restrict__ amax_bits,
+                                                     uint16_t* __restrict__ mubT = nullptr, int nkb16 = 0) {
   constexpr int SPLIT = 256 / D;  // threads per column
   const int j = blockIdx.x, bh = blockIdx.y;
   const int nkb = (S + 127) / 128;
@@ -350,6 +351,7 @@ __global__ void __launch_bounds__(256) vmeans_kernel(const uint16_t* __restrict_
     for (int q = 0; q < SPLIT; ++q) tot += sums[q][d];
     uint16_t b = demean ? f64_to_bf16_rne(tot / (double)n) : (uint16_t)0;
     mub[((int64_t)bh * nkb + j) * D + d] = b;
+    if (mubT) mubT[((int64_t)bh * D + d) * nkb16 + j] = b;  // [BH, D, nkb16]: the forward's flush operand
     mus[d] = bf16_bits_to_f32(b);
   }
   __syncthreads();
@@ -474,10 +476,10 @@ int prepare_launch(const PlanBuffers& p, const uint16_t* Q, const uint16_t* K, c
   // V' = V[pi]: block means, residual maximum per head, residual codes transposed
   if (cudaMemsetAsync(p.vamax, 0, sizeof(unsigned int) * BH, st) != cudaSuccess) return VC_ERR_CUDA;
   if (D == 128) {
-    vmeans_kernel<128><<<gblk, 256, 0, st>>>(V, perm, S, vsmooth ? 1 : 0, p.means, p.vamax);
+    vmeans_kernel<128><<<gblk, 256, 0, st>>>(V, perm, S, vsmooth ? 1 : 0, p.means, p.vamax, p.meansT, p.nkb16);
     vpack_kernel<128><<<gblk, 256, 0, st>>>(V, perm, S, S_pad, p.means, p.vamax, p.vcodes, p.vscales);
   } else {
-    vmeans_kernel<64><<<gblk, 256, 0, st>>>(V, perm, S, vsmooth ? 1 : 0, p.means, p.vamax);
+    vmeans_kernel<64><<<gblk, 256, 0, st>>>(V, perm, S, vsmooth ? 1 : 0, p.means, p.vamax, p.meansT, p.nkb16);
     vpack_kernel<64><<<gblk, 256, 0, st>>>(V, perm, S, S_pad, p.means, p.vamax, p.vcodes, p.vscales);
   }
   return check_launch();

@@ -158,3 +158,15 @@ def test_forced_timeout_reports_status_and_recovers(m):
     rel, _ = errors(f64(O[0, 0]), ref)
     assert rel <= FWD_ONLY_REL
     plan.destroy()
+
+
+def test_forward_is_deterministic(m):
+    """The forward has no data races: the same plan gives bitwise identical outputs."""
+    cfg = synth.config("small")
+    Q, K, V, plan = run(m, cfg, seed=9)
+    O1 = m.vc_attn_forward(plan).clone()
+    for _ in range(3):
+        O2 = m.vc_attn_forward(plan)
+        torch.cuda.synchronize()
+        assert torch.equal(O1.view(torch.int16), O2.view(torch.int16))
+    plan.destroy()
