@@ -42,6 +42,7 @@ VC_PLAN_VCODES = 7
 VC_PLAN_VSCALES = 8
 VC_PLAN_MEANS = 9
 VC_PLAN_CENTROIDS = 10
+VC_NOALLOC_MAX_HEADS = 4096
 
 EXPORTS = ("vc_attn_prepare", "vc_attn_prepare_ex", "vc_attn_forward", "vc_plan_size", "vc_plan_get",
            "vc_plan_status", "vc_plan_shape", "vc_plan_destroy", "vc_expcast_encode", "vc_strerror", "vc_version")
@@ -75,6 +76,7 @@ def lib() -> ctypes.CDLL:
         "vc_plan_shape": (i, [vp] + [ctypes.POINTER(i)] * 5),
         "vc_plan_destroy": (None, [vp]),
         "vc_expcast_encode": (i, [vp, vp, vp, ctypes.c_int64, vp, vp]),
+        "vc_residual_pack_noalloc": (i, [vp, vp, i, i, i, i, vp, vp, vp, vp]),
         "vc_strerror": (ctypes.c_char_p, [i]),
         "vc_version": (ctypes.c_char_p, []),
     }
@@ -216,6 +218,32 @@ def vc_plan_shape(plan: Plan) -> tuple[int, int, int, int, int]:
 
 def vc_plan_destroy(plan: Plan):
     plan.destroy()
+
+
+def vc_residual_pack_noalloc(V, perm, means, vcodes, vscales, stream=None):
+    """Value-side preparation into caller-provided tensors, with no device allocation.
+
+    For callers that must not allocate device memory: the library's only scratch is a fixed
+    in-library array of VC_NOALLOC_MAX_HEADS words per GPU. V: bf16 [B, H, S, D]; perm: int32
+    [B, H, S] or None (identity); means: bf16 [B, H, nkb, D]; vcodes: uint8 [B, H, D, S_pad];
+    vscales: fp32 [B, H] -- the layouts of VC_PLAN_MEANS / VC_PLAN_VCODES / VC_PLAN_VSCALES.
+    Calls that overlap on the GPU share that scratch and must be serialised by the caller.
+    """
+    if not (V.is_cuda and V.dtype == torch.bfloat16 and V.is_contiguous() and V.dim() == 4):
+        raise ValueError("V must be a contiguous CUDA bf16 tensor [B, H, S, D]")
+    B, H, S, D = V.shape
+    nkb = (S + 127) // 128
+    for t, dt, shape in ((means, torch.bfloat16, (B, H, nkb, D)), (vcodes, torch.uint8, (B, H, D, nkb * 128)),
+                         (vscales, torch.float32, (B, H))):
+        if not (t.is_cuda and t.dtype == dt and t.is_contiguous() and tuple(t.shape) == shape):
+            raise ValueError(f"output must be a contiguous CUDA {dt} tensor {shape}")
+    pp = None
+    if perm is not None:
+        if not (perm.is_cuda and perm.dtype == torch.int32 and perm.is_contiguous() and perm.numel() == B * H * S):
+            raise ValueError("perm must be a contiguous CUDA int32 tensor [B, H, S]")
+        pp = perm.data_ptr()
+    _check(lib().vc_residual_pack_noalloc(V.data_ptr(), pp, B, H, S, D, means.data_ptr(), vcodes.data_ptr(),
+                                          vscales.data_ptr(), _stream(stream)), "vc_residual_pack_noalloc")
 
 
 def vc_expcast_encode(s, a, b, stream=None):

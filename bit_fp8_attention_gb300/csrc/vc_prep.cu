@@ -486,3 +486,25 @@ int prepare_launch(const PlanBuffers& p, const uint16_t* Q, const uint16_t* K, c
 }
 
 }  // namespace vc
+
+namespace vc {
+
+// Block means and packed residual codes of V' = V[pi] with a caller-provided per-head scratch
+// word (the residual maximum). Used by the allocation-free entry point; the prepare step above
+// keeps using the plan's own scratch.
+int residual_pack_launch(const uint16_t* V, const int32_t* perm, int BH, int S, int D, uint16_t* means,
+                         uint8_t* vcodes, float* vscales, unsigned int* amax_scratch, cudaStream_t st) {
+  const int nkb = (S + 127) / 128, S_pad = nkb * 128;
+  dim3 gblk(nkb, BH);
+  if (cudaMemsetAsync(amax_scratch, 0, sizeof(unsigned int) * BH, st) != cudaSuccess) return VC_ERR_CUDA;
+  if (D == 128) {
+    vmeans_kernel<128><<<gblk, 256, 0, st>>>(V, perm, S, 1, means, amax_scratch);
+    vpack_kernel<128><<<gblk, 256, 0, st>>>(V, perm, S, S_pad, means, amax_scratch, vcodes, vscales);
+  } else {
+    vmeans_kernel<64><<<gblk, 256, 0, st>>>(V, perm, S, 1, means, amax_scratch);
+    vpack_kernel<64><<<gblk, 256, 0, st>>>(V, perm, S, S_pad, means, amax_scratch, vcodes, vscales);
+  }
+  return check_launch();
+}
+
+}  // namespace vc

@@ -144,6 +144,28 @@ void vc_plan_destroy(vc_plan* plan);
  * computed by the forward kernel's own code path.  s, a, b: device fp32 [n]; out: device u8. */
 int vc_expcast_encode(const float* s, const float* a, const float* b, int64_t n, uint8_t* out, cudaStream_t stream);
 
+/* ---- allocation-free variant ----------------------------------------------------------- */
+/* The pages have no counterpart to this call; it exists for callers that must not allocate
+ * device memory (for instance a framework whose memory pool already owns the whole device, or
+ * host code that may only allocate at start-up).
+ * vc_residual_pack_noalloc computes the value side of the prepare step -- for each (b, h), the
+ * gather V' = V[pi], the bf16 means of its 128-row blocks and the per-head E4M3 residual codes,
+ * transposed and zero-padded -- exactly as vc_attn_prepare_ex writes them into a plan
+ * (VC_PLAN_MEANS, VC_PLAN_VCODES, VC_PLAN_VSCALES), into buffers the caller provides.
+ * V: device bf16 [B, H, S, D]; perm: device int32 [B, H, S] (entries in [0, S)) or NULL for the
+ * identity; means: device bf16 [B, H, ceil(S/128), D]; vcodes: device uint8 [B, H, D, S_pad];
+ * vscales: device fp32 [B, H]. V, means and vcodes must be 16-byte aligned.
+ * It calls no cudaMalloc, cudaFree or allocating library routine. Its only scratch (one word per
+ * batch-head) is a fixed array inside the library, VC_NOALLOC_MAX_HEADS words per GPU, kept until
+ * the process exits: B*H above that limit returns VC_ERR_UNSUPPORTED. The first call on a device
+ * looks up that array's device address (once per device, with that device current); make that
+ * first call before any stream capture. Each call clears the scratch on `stream` before use, but
+ * all calls share it: calls that overlap on the GPU (other streams, other host threads) race and
+ * must be serialised by the caller. */
+#define VC_NOALLOC_MAX_HEADS 4096
+int vc_residual_pack_noalloc(const void* V, const int32_t* perm, int B, int H, int S, int D, void* means,
+                             uint8_t* vcodes, float* vscales, cudaStream_t stream);
+
 /* Human-readable text of a status code (static storage). */
 const char* vc_strerror(int status);
 /* Library version string. */
