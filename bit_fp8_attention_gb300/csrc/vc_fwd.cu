@@ -8,18 +8,21 @@
 // mid-window key order, packed transposed V.
 //
 // GB300 design (not the pages' kernel): one CTA per 128-row query tile and batch-head.
-//   warp 4      TMA producer: Q once; K' and V^T tiles of 128 keys into 3-stage rings; with
+//   producer    TMA: Q once; K' and V^T tiles of 128 keys into 3-stage rings; with
 //               V-Smooth, the transposed bf16 means of each 16-tile block run into a 2-stage ring.
-//   warp 5      MMA issuer (one thread): S = Q K'^T (kind::f8f6f4, SS) into one of two TMEM score
+//   MMA issuer  one thread: S = Q K'^T (kind::f8f6f4, SS) into one of two TMEM score
 //               buffers; O += P V and W += P E_{j mod 16} (TS: the codes P are read from TMEM),
 //               where E_s is a one-hot 16 x 128 block, so column j mod 16 of W receives the exact
 //               row sum of tile j; at the end of each run of tiles from one 16-tile block, the
 //               mean term O += F M^T (kind::f16, F = W / sV split into bf16 hi + lo, M the block's
 //               16 means) -- Eq. 6's r mu^T for 16 tiles at once, in the same accumulator.
-//   warps 0-3   softmax, one thread per query row: tile max on the raw scores, true-score max in
-//               code units, O/W rescale on every increase, E4M3 codes written into TMEM.
-// TMEM columns: O [0, D), W [D, D+16), F [D+16, D+32), P [160, 192) and [192, 224), score
-// buffers S [256, 384) and [384, 512).  P has its own columns so that the commit of S(p+2), which
+//   warps 0-7   softmax, two warpgroups on alternate key tiles, one thread per query row: tile max
+//               on the raw scores, true-score max in code units handed between the groups, O/W/l
+//               rescale on every increase, E4M3 codes written into TMEM.
+//   warp 8      TMA producer of Q and the K pairs; warp 10 TMA producer of V (with the one-hot rows)
+//               and the mean blocks; warp 9 MMA issuer.
+// TMEM columns: O [0, D), W [D, D+16), F [D+16, D+32), l [D+32], P [176, 208) and [208, 240),
+// score buffers S [256, 384) and [384, 512).  P has its own columns so that the commit of S(p+2), which
 // tracks every earlier MMA, also proves that PV(p) has finished reading P(p).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -36,22 +39,27 @@ constexpr float kFastMaxAbsM = 1048576.f;  // |M| below 2^20 code units: the one
 
 template <int D>
 struct FwdCfg {
-  static constexpr int NK = 3, NV = 3, NMU = 2;
-  static constexpr int QB = 128 * D;  // bytes of a Q or K tile (128 rows x D codes)
-  static constexpr int VB = D * 128;  // bytes of a V^T tile (D rows x 128 keys)
-  static constexpr int MUB = D * 32;  // bytes of a mean block (D rows x 16 bf16)
+  static constexpr int NKP = 2, NV = 3, NMU = 2;
+  static constexpr int QB = 128 * D;             // bytes of a Q or K tile (128 rows x D codes)
+  static constexpr int KPB = 2 * QB;             // a K stage: the two key tiles of one S pair
+  static constexpr int VB = D * 128;             // bytes of a V^T tile (D rows x 128 keys)
+  static constexpr int VSTAGE = (D + 16) * 128;  // V^T tile + 16 one-hot rows: the B operand of O|W += P [V; E]
+  static constexpr int MUB = D * 32;             // bytes of a mean block (D rows x 16 bf16)
   static constexpr uint32_t QK_LAYOUT = D == 128 ? kSw128 : kSw64;
   static constexpr uint32_t QK_SBO = 8 * D;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + QB;
-  static constexpr int OFF_V = OFF_K + NK * QB;
-  static constexpr int OFF_ONE = OFF_V + NV * VB;
-  static constexpr int OFF_MU = OFF_ONE + 16 * 2048;
+  static constexpr int OFF_V = OFF_K + NKP * KPB;
+  static constexpr int OFF_MU = OFF_V + NV * VSTAGE;
   static constexpr int OFF_BAR = OFF_MU + NMU * MUB;
-  static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 2 * NMU + 2 + 2 + 2 + 1 + 1;
+  static constexpr int NBAR = 1 + 2 * NKP + 2 * NV + 2 * NMU + 1 + 1 + 2 + 4 + 1 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + slack for aligning the base to 1024
-  static constexpr uint32_t T_O = 0, T_W = D, T_F = D + 16, T_P0 = 160, T_P1 = 192, T_S0 = 256, T_S1 = 384;
+  static constexpr int OFF_MBUF = OFF_MISC + 64;    // running max hand-off, 2 x 128 floats
+  static constexpr int OFF_MSEQ = OFF_MBUF + 1024;  // 4 publication counters
+  static constexpr int SMEM = OFF_MSEQ + 64 + 1024; // + slack for aligning the base to 1024
+  // TMEM columns: O|W [0, D+16), F [D+16, D+32), l [D+32], P0 [176, 208), P1 [208, 240),
+  // S pair [256, 512): the scores of tile 2k in [256, 384), of tile 2k+1 in [384, 512).
+  static constexpr uint32_t T_O = 0, T_W = D, T_F = D + 16, T_L = D + 32, T_P0 = 176, T_P1 = 208, T_S = 256;
 };
 
 struct FwdArgs {
@@ -178,147 +186,183 @@ __device__ __forceinline__ void store_flush_operand(uint32_t tF, const float (&w
 }
 
 template <int D>
-__global__ void __launch_bounds__(192, 1) vc_fwd_kernel(const __grid_constant__ FwdMaps maps, const FwdArgs args) {
+__global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ FwdMaps maps, const FwdArgs args) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base + C::OFF_Q;
   uint8_t* sK = base + C::OFF_K;
   uint8_t* sV = base + C::OFF_V;
-  uint8_t* sOne = base + C::OFF_ONE;
   uint8_t* sMu = base + C::OFF_MU;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::OFF_BAR);
   uint64_t* q_full = bars;
-  uint64_t* k_full = q_full + 1;
-  uint64_t* k_empty = k_full + C::NK;
-  uint64_t* v_full = k_empty + C::NK;
+  uint64_t* k_full = q_full + 1;          // per K pair stage
+  uint64_t* k_empty = k_full + C::NKP;
+  uint64_t* v_full = k_empty + C::NKP;
   uint64_t* v_empty = v_full + C::NV;
   uint64_t* mu_full = v_empty + C::NV;
   uint64_t* mu_empty = mu_full + C::NMU;
-  uint64_t* s_full = mu_empty + C::NMU;
-  uint64_t* p_full = s_full + 2;
-  // o_done[t & 1] completes when PV(t) and every earlier MMA are done. Two barriers alternating by
-  // tile: when the softmax waits for tile t, the same barrier's previous tile t-2 is known to be
-  // complete, so the barrier is never two phases away from the one waited for (parity waits only
-  // tell the current phase from the previous one).
+  uint64_t* s_full = mu_empty + C::NMU;   // S pair k landed (one phase per pair)
+  uint64_t* s_free = s_full + 1;          // both groups hold S pair k in registers (256 arrivals)
+  uint64_t* p_full = s_free + 1;          // per group: P of its tile written, O/W/l up to date
+  // o_done[t & 3] completes when PV(t) and every earlier MMA are done. Parity waits only tell the
+  // current phase from the previous one, so a wait for PV(v) must never find PV(v+4) complete too.
+  // A group at tile t waits only for v > t-5 (every PV up to t-4 is known complete from S, see
+  // below), and nothing past PV(t-1) can complete before this group's P(t) is published.
   uint64_t* o_done = p_full + 2;
-  uint64_t* f_full = o_done + 2;
+  uint64_t* f_full = o_done + 4;
   uint64_t* drain = f_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base + C::OFF_MISC + 8);
+  float* mbuf = reinterpret_cast<float*>(base + C::OFF_MBUF);
+  int* mseq = reinterpret_cast<int*>(base + C::OFF_MSEQ);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qt = blockIdx.x, bh = blockIdx.y;
   const int nkb = args.nkb;
+  const int npairs = (nkb + 1) / 2;
   const int start = (args.flags & VC_MIDWINDOW) ? min(nkb - 1, qt + 2) : -1;
   const bool use_mean = args.use_mean != 0;
 
   if (tid == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < C::NK; ++s) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
+    for (int s = 0; s < C::NKP; ++s) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
     for (int s = 0; s < C::NV; ++s) { mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1); }
     for (int s = 0; s < C::NMU; ++s) { mbar_init(&mu_full[s], 1); mbar_init(&mu_empty[s], 1); }
-    for (int b = 0; b < 2; ++b) { mbar_init(&s_full[b], 1); mbar_init(&p_full[b], 128); }
-    mbar_init(&o_done[0], 1);
-    mbar_init(&o_done[1], 1);
+    mbar_init(s_full, 1);
+    mbar_init(s_free, 256);
+    mbar_init(&p_full[0], 128);
+    mbar_init(&p_full[1], 128);
+    for (int i = 0; i < 4; ++i) mbar_init(&o_done[i], 1);
     mbar_init(f_full, 128);
     mbar_init(drain, 1);
     *abort_flag = 0;
+    for (int i = 0; i < 4; ++i) mseq[i] = 0;
     fence_mbar_init();
   }
-  // One-hot blocks E_s (16 rows x 128 keys, 128-byte swizzled rows): row s holds E4M3 1.0.
-  // A constant row is invariant under the 16-byte chunk swizzle, so it is written in place.
-  for (int i = tid; i < 16 * 128; i += blockDim.x) {
-    int blk = i >> 7, row = (i & 127) >> 3;
-    uint32_t v = (row == blk) ? 0x38383838u : 0u;
-    reinterpret_cast<uint4*>(sOne)[i] = make_uint4(v, v, v, v);
-  }
   if (warp == 0) tmem_alloc(tmem_slot, 512);
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-
-  if (warp == 4) {
-    // ------------------------------------------------------------------ TMA producer
+  if (warp == 8) {
+    // ------------------------------------------------------------------ K producer
+    // Q once, then the two key tiles of every S pair into a 2-stage ring; independent of the V
+    // ring, so the next pair is always in flight well before the MMA issuer needs it.
     if (lane == 0) {
       prefetch_tmap(&maps.q);
       prefetch_tmap(&maps.k);
-      prefetch_tmap(&maps.v);
-      if (use_mean) prefetch_tmap(&maps.mu);
-      const int row0 = bh * args.S_pad;
       mbar_arrive_expect_tx(q_full, C::QB);
-      tma_load_2d(sQ, &maps.q, 0, row0 + qt * 128, q_full);
-      int issued_k = 0, issued_v = 0, issued_mu = 0;
-      // The means of a block run are loaded when the run ends, just before the next run's first K
-      // tile: the ring stage they reuse was released by the mean MMA of the run two back, which the
-      // MMA thread issues before it can ever wait for that K tile.
-      auto load_mean_block = [&](int block) -> bool {
-        const int q = issued_mu, sm = q % C::NMU;
-        if (!wait_or_abort(&mu_empty[sm], ((q / C::NMU) & 1) ^ 1, kWaitLimit, abort_flag)) return false;
-        mbar_arrive_expect_tx(&mu_full[sm], C::MUB);
-        tma_load_2d(sMu + sm * C::MUB, &maps.mu, block * 16, bh * D, &mu_full[sm]);
-        issued_mu = q + 1;
-        return true;
-      };
+      tma_load_2d(sQ, &maps.q, 0, bh * args.S_pad + qt * 128, q_full);
+      const int row0 = bh * args.S_pad;
+      int issued_kp = 0;
       bool loads_ok = true;
-      for (int p = 0; p < nkb; ++p) {
+      for (int k = 0; k < npairs; ++k) {
         if (*abort_flag) { loads_ok = false; break; }
-        const int j = tile_at(p, start);
-        if (use_mean && p > 0 && seg_start(p, start) && !load_mean_block(tile_at(p - 1, start) >> 4)) {
-          record_failure(args.status, abort_flag, kStatusTimeoutLoad);
-          loads_ok = false;
-          break;
-        }
-        const int s = p % C::NK;
-        if (!wait_or_abort(&k_empty[s], ((p / C::NK) & 1) ^ 1, kWaitLimit, abort_flag)) {
-          record_failure(args.status, abort_flag, kStatusTimeoutLoad);
-          loads_ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(&k_full[s], C::QB);
-        tma_load_2d(sK + s * C::QB, &maps.k, 0, row0 + j * 128, &k_full[s]);
-        issued_k = p + 1;
-        const int sv = p % C::NV;
-        if (!wait_or_abort(&v_empty[sv], ((p / C::NV) & 1) ^ 1, kWaitLimit, abort_flag)) {
-          record_failure(args.status, abort_flag, kStatusTimeoutLoad);
-          loads_ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(&v_full[sv], C::VB);
-        tma_load_2d(sV + sv * C::VB, &maps.v, j * 128, bh * D, &v_full[sv]);
-        issued_v = p + 1;
+        const int s = k % C::NKP;
+        const int t0 = 2 * k, t1 = 2 * k + 1;
+        if (!wait_or_abort(&k_empty[s], ((k / C::NKP) & 1) ^ 1, kWaitLimit, abort_flag)) { loads_ok = false; break; }
+        mbar_arrive_expect_tx(&k_full[s], t1 < nkb ? 2 * C::QB : C::QB);
+        tma_load_2d(sK + s * C::KPB, &maps.k, 0, row0 + tile_at(t0, start) * 128, &k_full[s]);
+        if (t1 < nkb) tma_load_2d(sK + s * C::KPB + C::QB, &maps.k, 0, row0 + tile_at(t1, start) * 128, &k_full[s]);
+        issued_kp = k + 1;
       }
-      if (use_mean && loads_ok && !load_mean_block(tile_at(nkb - 1, start) >> 4))  // the last run
-        record_failure(args.status, abort_flag, kStatusTimeoutLoad);
+      if (!loads_ok) record_failure(args.status, abort_flag, kStatusTimeoutLoad);
       // Teardown: confirm that every load issued into this CTA's shared memory has landed.
       bool ok = mbar_wait(q_full, 0, kWaitLimit);
-      for (int p = max(0, issued_k - C::NK); p < issued_k; ++p)
-        ok &= mbar_wait(&k_full[p % C::NK], (p / C::NK) & 1, kWaitLimit);
-      for (int p = max(0, issued_v - C::NV); p < issued_v; ++p)
-        ok &= mbar_wait(&v_full[p % C::NV], (p / C::NV) & 1, kWaitLimit);
+      for (int k = max(0, issued_kp - C::NKP); k < issued_kp; ++k)
+        ok &= mbar_wait(&k_full[k % C::NKP], (k / C::NKP) & 1, kWaitLimit);
+      if (!ok) record_failure(args.status, abort_flag, kStatusTimeoutDrain);
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------------ V producer
+    // Lane 0 waits and issues the copies; the whole warp writes the 16 one-hot rows under each V^T
+    // tile (row j mod 16 holds E4M3 1.0), so that one MMA computes O += P V and W += P E at once.
+    // The means of a block run are loaded just before the V tile of the next run's first position:
+    // their ring stage was released by the mean MMA of the run two back, issued by the MMA thread
+    // before it needs any V tile from that position on.
+    const bool leader = lane == 0;
+    if (leader) {
+      prefetch_tmap(&maps.v);
+      if (use_mean) prefetch_tmap(&maps.mu);
+    }
+    int issued_v = 0, issued_mu = 0;
+    auto leader_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      bool ok = true;
+      if (leader) ok = wait_or_abort(bar, parity, kWaitLimit, abort_flag);
+      return __shfl_sync(0xffffffffu, ok, 0);
+    };
+    auto load_mean_block = [&](int block) -> bool {
+      const int q = issued_mu, sm = q % C::NMU;
+      if (!leader_wait(&mu_empty[sm], ((q / C::NMU) & 1) ^ 1)) return false;
+      if (leader) {
+        mbar_arrive_expect_tx(&mu_full[sm], C::MUB);
+        tma_load_2d(sMu + sm * C::MUB, &maps.mu, block * 16, bh * D, &mu_full[sm]);
+      }
+      issued_mu = q + 1;
+      return true;
+    };
+    bool loads_ok = true;
+    for (int t = 0; t < nkb && loads_ok; ++t) {
+      if (warp_aborted(abort_flag)) { loads_ok = false; break; }
+      const int j = tile_at(t, start);
+      if (use_mean && t > 0 && seg_start(t, start) && !load_mean_block(tile_at(t - 1, start) >> 4)) {
+        loads_ok = false;
+        break;
+      }
+      const int sv = t % C::NV;
+      if (!leader_wait(&v_empty[sv], ((t / C::NV) & 1) ^ 1)) { loads_ok = false; break; }
+      {  // one-hot rows: a constant row is invariant under the 16-byte chunk swizzle
+        uint4* onehot = reinterpret_cast<uint4*>(sV + sv * C::VSTAGE + C::VB);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int i = lane + 32 * q;
+          const uint32_t v = ((i >> 3) == (j & 15)) ? 0x38383838u : 0u;
+          onehot[i] = make_uint4(v, v, v, v);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+      }
+      if (leader) {
+        mbar_arrive_expect_tx(&v_full[sv], C::VB);
+        tma_load_2d(sV + sv * C::VSTAGE, &maps.v, j * 128, bh * D, &v_full[sv]);
+      }
+      issued_v = t + 1;
+    }
+    if (loads_ok && use_mean && !load_mean_block(tile_at(nkb - 1, start) >> 4)) loads_ok = false;  // the last run
+    if (!loads_ok && leader) record_failure(args.status, abort_flag, kStatusTimeoutLoad);
+    if (leader) {
+      bool ok = true;
+      for (int t = max(0, issued_v - C::NV); t < issued_v; ++t)
+        ok &= mbar_wait(&v_full[t % C::NV], (t / C::NV) & 1, kWaitLimit);
       for (int q = max(0, issued_mu - C::NMU); q < issued_mu; ++q)
         ok &= mbar_wait(&mu_full[q % C::NMU], (q / C::NMU) & 1, kWaitLimit);
       if (!ok) record_failure(args.status, abort_flag, kStatusTimeoutDrain);
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------------ MMA issuer
+    // Per pair k: once both groups hold S pair k in registers, S pair k+1 = Q K'(2k+2, 2k+3)^T as
+    // one N = 256 MMA group; then per tile t of the pair, the mean term of a finished block run and
+    // O|W += P(t) [V(t); E_{j mod 16}] as one N = D+16 MMA group.
     if (lane == 0) {
-      const uint32_t tO = tmem + C::T_O, tW = tmem + C::T_W, tF = tmem + C::T_F;
-      const uint32_t tS0 = tmem + C::T_S0, tS1 = tmem + C::T_S1, tP0 = tmem + C::T_P0, tP1 = tmem + C::T_P1;
-      constexpr uint32_t id_qk = idesc_e4m3(128, 128), id_pv = idesc_e4m3(128, D), id_w = idesc_e4m3(128, 16);
+      const uint32_t tO = tmem + C::T_O, tF = tmem + C::T_F, tS = tmem + C::T_S;
+      const uint32_t tP0 = tmem + C::T_P0, tP1 = tmem + C::T_P1;
+      constexpr uint32_t id_qk = idesc_e4m3(128, 256), id_pv = idesc_e4m3(128, D + 16);
       constexpr uint32_t id_mu = idesc_bf16(128, D);
-      auto issue_qk = [&](int p) -> bool {
-        const int s = p % C::NK;
-        if (!wait_or_abort(&k_full[s], (p / C::NK) & 1, kWaitLimit, abort_flag)) return false;
+      // Descriptors are built once; a stage or K step only adds to the start-address field
+      // (addresses are below 2^18, so the 14-bit field never carries).
+      const uint64_t dq = smem_desc(sQ, C::QK_SBO, C::QK_LAYOUT);
+      const uint64_t dk0 = smem_desc(sK, C::QK_SBO, C::QK_LAYOUT);
+      const uint64_t dv0 = smem_desc(sV, 1024, kSw128);
+      const uint64_t dmu0 = smem_desc(sMu, 256, kSw32);
+      auto issue_qk = [&](int k) -> bool {
+        const int s = k % C::NKP;
+        if (!wait_or_abort(&k_full[s], (k / C::NKP) & 1, kWaitLimit, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t dst = (p & 1) ? tS1 : tS0;
+        const uint64_t dk = dk0 + (uint64_t)(s * (C::KPB >> 4));
 #pragma unroll
-        for (int kk = 0; kk < D / 32; ++kk)
-          mma_e4m3_ss(dst, smem_desc(sQ + 32 * kk, C::QK_SBO, C::QK_LAYOUT),
-                      smem_desc(sK + s * C::QB + 32 * kk, C::QK_SBO, C::QK_LAYOUT), id_qk, kk > 0);
-        mma_commit(&s_full[p & 1]);
+        for (int kk = 0; kk < D / 32; ++kk) mma_e4m3_ss(tS, dq + 2 * kk, dk + 2 * kk, id_qk, kk > 0);
+        mma_commit(s_full);
         mma_commit(&k_empty[s]);
         return true;
       };
@@ -327,91 +371,107 @@ __global__ void __launch_bounds__(192, 1) vc_fwd_kernel(const __grid_constant__ 
         const int sm = q % C::NMU;
         if (!wait_or_abort(&mu_full[sm], (q / C::NMU) & 1, kWaitLimit, abort_flag)) return false;
         tc_fence_after();
-        const uint64_t bdesc = smem_desc(sMu + sm * C::MUB, 256, kSw32);
+        const uint64_t bdesc = dmu0 + (uint64_t)(sm * (C::MUB >> 4));
         mma_bf16_ts(tO, tF, bdesc, id_mu, 1);
         mma_bf16_ts(tO, tF + 8, bdesc, id_mu, 1);
         mma_commit(&mu_empty[sm]);
         return true;
       };
-      bool ok = mbar_wait(q_full, 0, kWaitLimit);
-      if (ok) ok = issue_qk(0);
-      if (ok && nkb > 1) ok = issue_qk(1);
+      bool ok = mbar_wait(q_full, 0, kWaitLimit) && issue_qk(0);
       if (!ok) record_failure(args.status, abort_flag, kStatusTimeoutLoad);
       int seg = -1;  // ordinal of the current block run
-      for (int p = 0; ok && p < nkb; ++p) {
+      for (int k = 0; ok && k < npairs; ++k) {
         if (*abort_flag) { ok = false; break; }
-        const int b = p & 1;
-        if (!wait_or_abort(&p_full[b], (p >> 1) & 1, kWaitLimit, abort_flag)) {
-          record_failure(args.status, abort_flag, kStatusTimeoutP);
-          ok = false;
-          break;
-        }
-        const bool fresh = seg_start(p, start);
-        if (fresh) {
-          if (use_mean && seg >= 0 && !issue_mean(seg)) {
+        if (k + 1 < npairs) {
+          if (!wait_or_abort(s_free, k & 1, kWaitLimit, abort_flag)) {
+            record_failure(args.status, abort_flag, kStatusTimeoutP);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (!issue_qk(k + 1)) {
             record_failure(args.status, abort_flag, kStatusTimeoutLoad);
             ok = false;
             break;
           }
-          ++seg;
         }
-        const int sv = p % C::NV;
-        if (!wait_or_abort(&v_full[sv], (p / C::NV) & 1, kWaitLimit, abort_flag)) {
-          record_failure(args.status, abort_flag, kStatusTimeoutLoad);
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t tP = b ? tP1 : tP0;
+        for (int t = 2 * k; ok && t <= 2 * k + 1 && t < nkb; ++t) {
+          const int g = t & 1;
+          if (!wait_or_abort(&p_full[g], k & 1, kWaitLimit, abort_flag)) {
+            record_failure(args.status, abort_flag, kStatusTimeoutP);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (seg_start(t, start)) {
+            if (use_mean && seg >= 0 && !issue_mean(seg)) {
+              record_failure(args.status, abort_flag, kStatusTimeoutLoad);
+              ok = false;
+              break;
+            }
+            ++seg;
+          }
+          const int sv = t % C::NV;
+          if (!wait_or_abort(&v_full[sv], (t / C::NV) & 1, kWaitLimit, abort_flag)) {
+            record_failure(args.status, abort_flag, kStatusTimeoutLoad);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t tP = g ? tP1 : tP0;
+          const uint64_t dv = dv0 + (uint64_t)(sv * (C::VSTAGE >> 4));
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_e4m3_ts(tO, tP + 8 * kk, smem_desc(sV + sv * C::VB + 32 * kk, 1024, kSw128), id_pv,
-                      (p > 0 || kk > 0));
-        const uint8_t* one = sOne + (tile_at(p, start) & 15) * 2048;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_e4m3_ts(tW, tP + 8 * kk, smem_desc(one + 32 * kk, 1024, kSw128), id_w, (!fresh || kk > 0));
-        mma_commit(&o_done[p & 1]);
-        mma_commit(&v_empty[sv]);
-        if (p + 2 < nkb && !issue_qk(p + 2)) {
-          record_failure(args.status, abort_flag, kStatusTimeoutLoad);
-          ok = false;
-          break;
+          for (int kk = 0; kk < 4; ++kk) mma_e4m3_ts(tO, tP + 8 * kk, dv + 2 * kk, id_pv, (t > 0 || kk > 0));
+          mma_commit(&o_done[t & 3]);
+          mma_commit(&v_empty[sv]);
         }
       }
       if (ok && use_mean && !*abort_flag) {  // the last block run: its F arrives after the loop
         if (!wait_or_abort(f_full, 0, kWaitLimit, abort_flag) || !issue_mean(seg))
           record_failure(args.status, abort_flag, kStatusTimeoutP);
         else
-          mma_commit(&o_done[nkb & 1]);  // as if it were tile nkb
+          mma_commit(&o_done[nkb & 3]);  // as if it were tile nkb
       }
       // Teardown: every MMA this thread issued has completed before TMEM is released.
       mma_commit(drain);
       if (!mbar_wait(drain, 0, kWaitLimit)) record_failure(args.status, abort_flag, kStatusTimeoutDrain);
     }
-  } else {
-    // ------------------------------------------------------------------ softmax warps 0-3
-    const int row = tid;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  } else if (warp < 8) {
+    // ------------------------------------------------------------------ softmax warps 0-7
+    // Group g takes tile t = 2k + g of every S pair k, one thread per query row, its 128 scores
+    // held in registers. The running max passes from one group to the next through shared memory
+    // (published with a release store of the position). O, W and the row sum l (one TMEM column)
+    // are touched only after PV of the previous tile has completed, which orders both groups'
+    // updates; the rescale is done after the codes, so the wait for PV(t-1) overlaps the coding.
+    const int wg = warp >> 2, wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const uint32_t tO = tmem + lane_base + C::T_O, tW = tmem + lane_base + C::T_W, tF = tmem + lane_base + C::T_F;
-    const uint32_t tS0 = tmem + lane_base + C::T_S0, tS1 = tmem + lane_base + C::T_S1;
-    const uint32_t tP0 = tmem + lane_base + C::T_P0, tP1 = tmem + lane_base + C::T_P1;
+    const uint32_t tL = tmem + lane_base + C::T_L;
+    const uint32_t tS = tmem + lane_base + C::T_S + 128 * wg;
+    const uint32_t tP = tmem + lane_base + (wg ? C::T_P1 : C::T_P0);
     const float* skh = args.kscales + (int64_t)bh * nkb;
     const float aq = args.code_scale * args.qscales[(int64_t)bh * nkb + qt];
     const float sv = args.vscales[bh];
     const float inv_sv = 1.f / sv;
     const bool expcast = (args.flags & VC_EXPCAST) != 0;
     const int tail_valid = args.S - (nkb - 1) * 128;
-    float M = -INFINITY, l = 0.f;
     bool ok = true;
-    float sk_next = skh[tile_at(0, start)];
+    int known = -1;  // every PV up to this tile is known complete
+    float sk_next = wg < nkb ? skh[tile_at(wg, start)] : 1.f;
 
-    // PV(t) and everything before it done. Only called for t = p-1 at tile p (or t = nkb-1, nkb at
-    // the end), when tile t-2 is already known to be complete.
     auto wait_o = [&](int t) -> bool {
-      if (!warp_wait(&o_done[t & 1], (t >> 1) & 1, kWaitLimit, abort_flag)) {
+      if (!warp_wait(&o_done[t & 3], (t >> 2) & 1, kWaitLimit, abort_flag)) {
         record_failure(args.status, abort_flag, kStatusTimeoutO);
         return false;
+      }
+      return true;
+    };
+    // PV(u) and everything before it complete, waiting tile by tile from the last known one.
+    auto ensure_pv = [&](int u) -> bool {
+      for (int v = known + 1; v <= u; ++v) {
+        if (!wait_o(v)) return false;
+        known = v;
       }
       tc_fence_after();
       return true;
@@ -423,49 +483,58 @@ __global__ void __launch_bounds__(192, 1) vc_fwd_kernel(const __grid_constant__ 
 #pragma unroll
       for (int s = 0; s < 16; ++s) w[s] = __uint_as_float(wr[s]);
     };
-
-    for (int p = 0; p < nkb; ++p) {
-      if (warp_aborted(abort_flag)) { ok = false; break; }
-      const int j = tile_at(p, start);
-      const int b = p & 1;
-      const uint32_t tS = b ? tS1 : tS0, tP = b ? tP1 : tP0;
-      const float sk = sk_next;
-      if (p + 1 < nkb) sk_next = skh[tile_at(p + 1, start)];
-      // A new block run: the previous run's row sums (complete once PV(p-1) is done) leave W.
-      const bool flush = p > 0 && seg_start(p, start);
-      bool o_ready = false;
-      float w[16];
-      if (flush) {
-        if (!wait_o(p - 1)) { ok = false; break; }
-        o_ready = true;
-        read_w(w);
-        float ws = 0.f;
-#pragma unroll
-        for (int s = 0; s < 16; ++s) ws += w[s];
-        l += ws;
+    // Wait (bounded) until the running max after position t-1 has been published.
+    auto wait_max = [&](int t) -> bool {
+      bool got = true;
+      if (lane == 0) {
+        got = false;
+        for (uint32_t i = 0; i < (kWaitLimit << 6); ++i) {
+          if (ld_acquire_cta(&mseq[wq]) >= t) { got = true; break; }
+          if ((i & 255u) == 255u && *abort_flag) break;
+        }
       }
-      const uint32_t lim = (p == 0 && (args.flags & VC_DEBUG_TIMEOUT)) ? 0u : kWaitLimit;
-      if (!warp_wait(&s_full[b], (p >> 1) & 1, lim, abort_flag)) {
+      got = __shfl_sync(0xffffffffu, got, 0);
+      __syncwarp();
+      return got;
+    };
+
+    if (wg == 0) {  // l starts at 0
+      tmem_st1(tL, 0u);
+      tmem_wait_st();
+    }
+
+    for (int k = 0; ok; ++k) {
+      const int t = 2 * k + wg;
+      if (t >= nkb) break;
+      if (warp_aborted(abort_flag)) { ok = false; break; }
+      const int j = tile_at(t, start);
+      const float sk = sk_next;
+      if (t + 2 < nkb) sk_next = skh[tile_at(t + 2, start)];
+      const uint32_t lim = (t == 0 && (args.flags & VC_DEBUG_TIMEOUT)) ? 0u : kWaitLimit;
+      if (!warp_wait(s_full, k & 1, lim, abort_flag)) {
         record_failure(args.status, abort_flag, kStatusTimeoutS);
         ok = false;
         break;
       }
       tc_fence_after();
+      known = max(known, 2 * k - 3);  // S pair k was issued after PV(2k-3)
       uint32_t sr[128];
       tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
       tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
       tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
       tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(s_free);  // the next S pair may overwrite the score buffers
       float s[128];
 #pragma unroll
       for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
-      if (j == nkb - 1 && tail_valid < 128) {
+      if (j == nkb - 1 && tail_valid < 128) {  // keys past S: -inf for the max, code 0
 #pragma unroll
         for (int c = 0; c < 128; ++c)
           if (c >= tail_valid) s[c] = -INFINITY;
       }
-      // Row max of the raw scores: eight independent chains, then a short tree.
+      // Row max of the raw scores: eight independent max3 chains, then a short tree.
       float m8[8];
 #pragma unroll
       for (int g = 0; g < 8; ++g) {
@@ -476,68 +545,100 @@ __global__ void __launch_bounds__(192, 1) vc_fwd_kernel(const __grid_constant__ 
       }
       const float mx = fmaxf(max3f(m8[0], m8[1], m8[2]), max3f(max3f(m8[3], m8[4], m8[5]), m8[6], m8[7]));
       const float aj = aq * sk;
-      const float t = mx * aj;  // = max_c fl(s_c * a_j): rounding is monotone and a_j > 0
-      const float Mn = fmaxf(M, t);
+      const float tmax = mx * aj;  // = max_c fl(s_c * a_j): rounding is monotone and a_j > 0
+      float M = -INFINITY;
+      if (t > 0) {
+        if (!wait_max(t)) {
+          record_failure(args.status, abort_flag, kStatusTimeoutS);
+          ok = false;
+          break;
+        }
+        M = mbuf[((t - 1) & 1) * 128 + row];
+      }
+      const float Mn = fmaxf(M, tmax);
+      if (t + 1 < nkb) {  // hand the running max to the other group as early as possible
+        mbuf[(t & 1) * 128 + row] = Mn;
+        __syncwarp();
+        if (lane == 0) st_release_cta(&mseq[wq], t + 1);
+      }
+      // Codes. P(t) reuses the columns of P(t-2), which PV(t-2) must have read.
+      if (!ensure_pv(t - 2)) { ok = false; break; }
+      const float bb = __fsub_rn(kB0, Mn);
+      const bool fast = expcast && __all_sync(0xffffffffu, fabsf(Mn) < kFastMaxAbsM);
+      const uint64_t a2 = pack2f(aj, aj), b2 = pack2f(bb, bb);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[16];
+        if (fast) {
+#pragma unroll
+          for (int g = 0; g < 16; ++g) {
+            const int c = 64 * h + 4 * g;
+            pk[g] = expcast4(s[c], s[c + 1], s[c + 2], s[c + 3], a2, a2, b2, b2);
+          }
+        } else if (expcast) {
+#pragma unroll
+          for (int g = 0; g < 16; ++g) {
+            const int c = 64 * h + 4 * g;
+            pk[g] = pack4(expcast_code(s[c], aj, bb), expcast_code(s[c + 1], aj, bb), expcast_code(s[c + 2], aj, bb),
+                          expcast_code(s[c + 3], aj, bb));
+          }
+        } else {
+#pragma unroll
+          for (int g = 0; g < 16; ++g) {
+            const int c = 64 * h + 4 * g;
+            pk[g] = pack4(expcast_off_code(s[c], aj, bb), expcast_off_code(s[c + 1], aj, bb),
+                          expcast_off_code(s[c + 2], aj, bb), expcast_off_code(s[c + 3], aj, bb));
+          }
+        }
+        tmem_st16(tP + 16 * h, pk);
+      }
+      // A new block run: the previous run's row sums (complete once PV(t-1) is done) leave W.
+      // Every max increase rescales O, W and l by alpha = 2^((M - M')/8).
       const bool inc = (Mn > M) && (M > -INFINITY);
-      float alpha = 1.f;
-      if (__any_sync(0xffffffffu, inc)) {
-        if (p > 0 && !o_ready) {
-          if (!wait_o(p - 1)) { ok = false; break; }
-          o_ready = true;
+      const bool flush = t > 0 && seg_start(t, start);
+      const bool any_inc = __any_sync(0xffffffffu, inc);
+      if (flush || any_inc) {
+        if (!ensure_pv(t - 1)) { ok = false; break; }
+        const float alpha = inc ? ex2_approx(__fmul_rn(__fsub_rn(M, Mn), 0.125f)) : 1.f;
+        float w[16];
+        float ws = 0.f;
+        if (flush) {  // take the run's row sums out of W and restart it at zero
+          read_w(w);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) ws += w[i];
+          const uint32_t zero[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+          tmem_st16(tW, zero);
         }
-        alpha = inc ? ex2_approx(__fmul_rn(__fsub_rn(M, Mn), 0.125f)) : 1.f;
-        l *= alpha;
+        const float lv = __uint_as_float(tmem_ld1(tL));
+        tmem_wait_ld();
+        if (any_inc) {
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t o[32];
-          tmem_ld32(tO + c0, o);
-          tmem_wait_ld();
+          for (int c0 = 0; c0 < (flush ? D : D + 16); c0 += 16) {
+            uint32_t o[16];
+            tmem_ld16(tO + c0, o);
+            tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(tO + c0, o);
+            for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st16(tO + c0, o);
+          }
         }
-        if (!flush) {  // a flushed W is about to be overwritten by this tile's row sums
-          uint32_t wr[16];
-          tmem_ld16(tW, wr);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) wr[i] = __float_as_uint(__uint_as_float(wr[i]) * alpha);
-          tmem_st16(tW, wr);
-        }
+        tmem_st1(tL, __float_as_uint((lv + ws) * alpha));
+        if (flush && use_mean) store_flush_operand(tF, w, inv_sv * alpha);
       }
-      if (flush && use_mean) store_flush_operand(tF, w, inv_sv * alpha);
-      M = Mn;
-      const float bb = __fsub_rn(kB0, M);
-      uint32_t pk[32];
-      if (expcast && __all_sync(0xffffffffu, fabsf(M) < kFastMaxAbsM)) {
-        const uint64_t a2 = pack2f(aj, aj), b2 = pack2f(bb, bb);
-#pragma unroll
-        for (int g = 0; g < 32; ++g)
-          pk[g] = expcast4(s[4 * g], s[4 * g + 1], s[4 * g + 2], s[4 * g + 3], a2, a2, b2, b2);
-      } else if (expcast) {
-#pragma unroll
-        for (int g = 0; g < 32; ++g)
-          pk[g] = pack4(expcast_code(s[4 * g], aj, bb), expcast_code(s[4 * g + 1], aj, bb),
-                        expcast_code(s[4 * g + 2], aj, bb), expcast_code(s[4 * g + 3], aj, bb));
-      } else {
-#pragma unroll
-        for (int g = 0; g < 32; ++g)
-          pk[g] = pack4(expcast_off_code(s[4 * g], aj, bb), expcast_off_code(s[4 * g + 1], aj, bb),
-                        expcast_off_code(s[4 * g + 2], aj, bb), expcast_off_code(s[4 * g + 3], aj, bb));
-      }
-      tmem_st32(tP, pk);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&p_full[b]);
+      mbar_arrive(&p_full[wg]);
     }
 
-    if (ok && !warp_aborted(abort_flag) && wait_o(nkb - 1)) {
+    // Group 0 finishes: every PV done, the last run's row sums and means, then O = sV A / l.
+    if (wg == 0 && ok && !warp_aborted(abort_flag) && ensure_pv(nkb - 1)) {
       float w[16];
       read_w(w);
       float ws = 0.f;
 #pragma unroll
-      for (int s = 0; s < 16; ++s) ws += w[s];
-      l += ws;
+      for (int i = 0; i < 16; ++i) ws += w[i];
+      const float l = __uint_as_float(tmem_ld1(tL)) + ws;
+      tmem_wait_ld();
       bool ready = true;
       if (use_mean) {  // the last block run's mean term, then the accumulator is final
         store_flush_operand(tF, w, inv_sv);
@@ -545,6 +646,7 @@ __global__ void __launch_bounds__(192, 1) vc_fwd_kernel(const __grid_constant__ 
         tc_fence_before();
         mbar_arrive(f_full);
         ready = wait_o(nkb);
+        tc_fence_after();
       }
       if (ready) {
         const float scale = sv / l;
@@ -648,7 +750,7 @@ static int launch_fwd(const PlanBuffers& p, const FwdMaps& maps, uint16_t* O, un
   a.code_scale = (float)(8.0 * 1.4426950408889634 / __builtin_sqrt((double)D));
   a.use_mean = (p.has_means && (flags & VC_VSMOOTH)) ? 1 : 0;
   dim3 grid(p.nkb, p.B * p.H);
-  vc_fwd_kernel<D><<<grid, 192, C::SMEM, st>>>(maps, a);
+  vc_fwd_kernel<D><<<grid, 352, C::SMEM, st>>>(maps, a);
   return cudaPeekAtLastError() == cudaSuccess ? VC_OK : VC_ERR_CUDA;
 }
 

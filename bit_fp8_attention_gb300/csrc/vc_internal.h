@@ -4,7 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/vc_attn.h"
+#include "vc_attn.h"
 
 namespace vc {
 

@@ -170,3 +170,29 @@ def test_forward_is_deterministic(m):
         torch.cuda.synchronize()
         assert torch.equal(O1.view(torch.int16), O2.view(torch.int16))
     plan.destroy()
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_repeated_launches_never_stall(m, D):
+    """Many back-to-back launches over every flag combination finish without a wait running out.
+
+    The softmax groups, the MMA thread and the two load warps hand tiles around through mbarrier
+    phases; a parity wait that could see its barrier two phases ahead would stall only under some
+    interleavings, so the check is statistical: 4 flag sets x 12 launches on a 256-tile sequence.
+    """
+    S = 32768
+    cfg = synth.custom(S=S, D=D, H=4, k=S // 128, iters=2)
+    Q, K, V = synth.make_inputs(cfg, seed=21, device="cuda")
+    plan = m.vc_attn_prepare(Q, K, V, cfg["k"], cfg["iters"])
+    base = m.VC_EXPCAST | m.VC_VSMOOTH | m.VC_MIDWINDOW
+    for flags in (base, base & ~m.VC_MIDWINDOW, base & ~m.VC_VSMOOTH, m.VC_EXPCAST):
+        ref = None
+        for rep in range(12):
+            O = m.vc_attn_forward(plan, flags=flags)
+            rc, bits = m.vc_plan_status(plan)
+            assert rc == 0 and bits == 0, f"flags {flags} launch {rep}: status bits {bits}"
+            if ref is None:
+                ref = O.clone()
+            else:
+                assert torch.equal(ref.view(torch.int16), O.view(torch.int16)), f"flags {flags} launch {rep}"
+    plan.destroy()
