@@ -123,8 +123,9 @@ class ClockSampler:
 
 
 def launches_per_step(cfg) -> int:
-    # prepare: Q quant, k-means init, (assign, argsort, update) x iters, K' quant, means, residual pack
-    return 5 + 3 * cfg["iters"] + 1  # + the fused forward
+    # prepare: Q quant, k-means init, (assign, label histogram, scan, scatter, update) x iters,
+    # K' quant, block means, residual pack; then the fused forward
+    return 5 + 5 * cfg["iters"] + 1
 
 
 def cpu_baseline(cfg, Q, K, V, budget_rows: int = 48):

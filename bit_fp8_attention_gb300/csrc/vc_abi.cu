@@ -55,6 +55,8 @@ int plan_create(int B, int H, int S, int D, int k, vc_plan** out) {
   b.nkb = (S + 127) / 128;
   b.S_pad = b.nkb * 128;
   b.nkb16 = (b.nkb + 15) / 16 * 16;
+  b.kpad = (k + 127) / 128 * 128;
+  b.nchunk = vc::kmeans_chunks(S);
   const size_t BH = (size_t)B * H;
   const size_t codes = BH * b.S_pad * D;
   const size_t sizes[] = {
@@ -72,6 +74,9 @@ int plan_create(int B, int H, int S, int D, int k, vc_plan** out) {
       BH * k * 4,                     // cnorm
       BH * k * 4,                     // counts
       BH * k * 4,                     // offsets
+      BH * 2 * b.kpad * D * 2,        // cent16
+      BH * b.kpad * 4,                // cnormp
+      BH * b.nchunk * k * 4,          // chist
       BH * 4,                         // vamax
       16,                             // status
   };
@@ -87,7 +92,8 @@ int plan_create(int B, int H, int S, int D, int k, vc_plan** out) {
   void** slots[] = {(void**)&b.qcodes, (void**)&b.qscales, (void**)&b.kcodes, (void**)&b.kscales,
                     (void**)&b.vcodes, (void**)&b.vscales, (void**)&b.means,   (void**)&b.meansT, (void**)&b.labels,
                     (void**)&b.perm,   (void**)&b.cent,    (void**)&b.cnorm,   (void**)&b.counts,
-                    (void**)&b.offsets, (void**)&b.vamax,  (void**)&b.status};
+                    (void**)&b.offsets, (void**)&b.cent16, (void**)&b.cnormp,  (void**)&b.chist,
+                    (void**)&b.vamax,  (void**)&b.status};
   for (size_t i = 0; i < sizeof(sizes) / sizeof(sizes[0]); ++i) {
     *slots[i] = p;
     p += align_up(sizes[i]);

@@ -701,8 +701,8 @@ static EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-static int encode_2d(CUtensorMap* m, CUtensorMapDataType dt, void* base, uint64_t inner, uint64_t rows,
-                     uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw) {
+int encode_2d(CUtensorMap* m, CUtensorMapDataType dt, void* base, uint64_t inner, uint64_t rows,
+              uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return VC_ERR_CUDA;
   cuuint64_t gd[2] = {inner, rows};

@@ -24,6 +24,11 @@ struct PlanBuffers {
   int32_t* perm;        // [BH, S]
   float* cent;          // [BH, k, D]
   float* cnorm;         // [BH, k]
+  int kpad;             // k rounded up to a multiple of 128
+  int nchunk;           // argsort chunks per head
+  uint16_t* cent16;     // [BH, 2, kpad, D] bf16 hi and lo parts of the centroids (pad rows 0)
+  float* cnormp;        // [BH, kpad] squared centroid norms, +inf on the pad rows
+  int32_t* chist;       // [BH, nchunk, k] per-chunk label counts, then chunk start positions
   int32_t* counts;      // [BH, k]
   int32_t* offsets;     // [BH, k]
   unsigned int* vamax;  // [BH] residual |max| as float bits
@@ -33,6 +38,13 @@ struct PlanBuffers {
 
 int prepare_launch(const PlanBuffers& p, const uint16_t* Q, const uint16_t* K, const uint16_t* V,
                    const int32_t* perm_in, bool vsmooth, int iters, cudaStream_t st);
+
+int kmeans_launch(const PlanBuffers& p, const uint16_t* V, int iters, cudaStream_t st);
+int kmeans_chunks(int S);
+
+// cuTensorMapEncodeTiled on a 2-D row-major tensor (rows x inner elements, row pitch in bytes).
+int encode_2d(CUtensorMap* m, CUtensorMapDataType dt, void* base, uint64_t inner, uint64_t rows,
+              uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw);
 
 struct FwdMaps {
   CUtensorMap q, k, v, mu;

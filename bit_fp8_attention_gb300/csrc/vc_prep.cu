@@ -109,210 +109,6 @@ __global__ void __launch_bounds__(256) quant_blocks_kernel(const uint16_t* __res
   }
 }
 
-// ---------------------------------------------------------------------------------------------
-// k-means.  Reading of "online k-means" (VC-Attention Sec. 3.2): Lloyd rounds run at inference
-// time; centroids start at the rows floor(i*S/k); assignment to the nearest centroid in squared
-// Euclidean distance (evaluated as ||c||^2 - 2 x.c in fp32; near-ties may resolve differently
-// from an fp64 evaluation); update = member mean (fp64 sums), an empty cluster keeps its centroid.
-// ---------------------------------------------------------------------------------------------
-__global__ void kmeans_init_kernel(const uint16_t* __restrict__ v, int S, int D, int k, float* __restrict__ cent,
-                                   float* __restrict__ cnorm) {
-  const int i = blockIdx.x, bh = blockIdx.y;
-  const int64_t src = (int64_t)i * S / k;
-  const uint16_t* row = v + ((int64_t)bh * S + src) * D;
-  float* c = cent + ((int64_t)bh * k + i) * D;
-  float acc = 0.f;
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    float x = bf16_bits_to_f32(row[d]);
-    c[d] = x;
-    acc = fmaf(x, x, acc);
-  }
-  __shared__ float red[32];
-  for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float s = 0.f;
-    for (int w = 0; w < (int)(blockDim.x + 31) / 32; ++w) s += red[w];
-    cnorm[(int64_t)bh * k + i] = s;
-  }
-}
-
-// Tile: 64 tokens x 64 centroids per step, 256 threads, 4 x 4 register tile per thread.
-template <int D>
-constexpr int kmeans_assign_smem() { return (D * (64 + 4) * 2 + 16 * 64 * 2) * 4; }
-
-template <int D>
-__global__ void __launch_bounds__(256) kmeans_assign_kernel(const uint16_t* __restrict__ v, int S, int k,
-                                                            const float* __restrict__ cent,
-                                                            const float* __restrict__ cnorm,
-                                                            int32_t* __restrict__ labels) {
-  constexpr int TT = 64, TC = 64;
-  extern __shared__ float kmeans_smem[];
-  float(*xs)[TT + 4] = reinterpret_cast<float(*)[TT + 4]>(kmeans_smem);            // xs[d][token]
-  float(*cs)[TC + 4] = reinterpret_cast<float(*)[TC + 4]>(kmeans_smem + D * (TT + 4));  // cs[d][centroid]
-  float(*bestd)[TT] = reinterpret_cast<float(*)[TT]>(kmeans_smem + D * (TT + 4) + D * (TC + 4));
-  int(*besti)[TT] = reinterpret_cast<int(*)[TT]>(kmeans_smem + D * (TT + 4) + D * (TC + 4) + 16 * TT);
-  const int bh = blockIdx.y;
-  const int t0 = blockIdx.x * TT;
-  const int tid = threadIdx.x;
-  const int tr = tid / 16, tc = tid % 16;  // token group (4 tokens), centroid group (4 centroids)
-  const uint16_t* vh = v + (int64_t)bh * S * D;
-  for (int e = tid; e < TT * D; e += 256) {
-    int r = e / D, d = e % D;
-    int t = t0 + r;
-    xs[d][r] = t < S ? bf16_bits_to_f32(vh[(int64_t)t * D + d]) : 0.f;
-  }
-  float bd[4];
-  int bi[4];
-#pragma unroll
-  for (int a = 0; a < 4; ++a) { bd[a] = INFINITY; bi[a] = 0; }
-  const float* ch = cent + (int64_t)bh * k * D;
-  const float* nh = cnorm + (int64_t)bh * k;
-  for (int c0 = 0; c0 < k; c0 += TC) {
-    __syncthreads();
-    for (int e = tid; e < TC * D; e += 256) {
-      int r = e / D, d = e % D;
-      cs[d][r] = (c0 + r) < k ? ch[(int64_t)(c0 + r) * D + d] : 0.f;
-    }
-    __syncthreads();
-    float acc[4][4];
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-      for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
-#pragma unroll 8
-    for (int d = 0; d < D; ++d) {
-      float xa[4], cb[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) xa[a] = xs[d][tr * 4 + a];
-#pragma unroll
-      for (int b = 0; b < 4; ++b) cb[b] = cs[d][tc * 4 + b];
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(xa[a], cb[b], acc[a][b]);
-    }
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      int ci = c0 + tc * 4 + b;
-      if (ci < k) {
-        float cn = nh[ci];
-#pragma unroll
-        for (int a = 0; a < 4; ++a) {
-          float dist = fmaf(-2.f, acc[a][b], cn);
-          if (dist < bd[a]) { bd[a] = dist; bi[a] = ci; }
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int a = 0; a < 4; ++a) {
-    bestd[tc][tr * 4 + a] = bd[a];
-    besti[tc][tr * 4 + a] = bi[a];
-  }
-  __syncthreads();
-  if (tid < TT) {
-    float b = bestd[0][tid];
-    int i = besti[0][tid];
-    for (int g = 1; g < 16; ++g) {  // lexicographic (distance, index): ties go to the lowest index
-      float d2 = bestd[g][tid];
-      int i2 = besti[g][tid];
-      if (d2 < b || (d2 == b && i2 < i)) { b = d2; i = i2; }
-    }
-    int t = t0 + tid;
-    if (t < S) labels[(int64_t)bh * S + t] = i;
-  }
-}
-
-// Stable counting sort of the labels of one batch-head: counts, exclusive offsets, and the
-// permutation listing cluster 0's tokens in token order, then cluster 1's, ...
-__global__ void __launch_bounds__(1024) argsort_kernel(const int32_t* __restrict__ labels, int S, int k,
-                                                       int32_t* __restrict__ perm, int32_t* __restrict__ counts,
-                                                       int32_t* __restrict__ offsets) {
-  __shared__ int hist[1024];
-  __shared__ int off[1024];
-  const int bh = blockIdx.x;
-  const int32_t* z = labels + (int64_t)bh * S;
-  for (int i = threadIdx.x; i < k; i += blockDim.x) hist[i] = 0;
-  __syncthreads();
-  for (int t = threadIdx.x; t < S; t += blockDim.x) atomicAdd(&hist[z[t]], 1);
-  __syncthreads();
-  if (threadIdx.x < 32) {  // exclusive scan by one warp over k <= 1024 entries
-    int carry = 0;
-    for (int base = 0; base < k; base += 32) {
-      int i = base + threadIdx.x;
-      int val = i < k ? hist[i] : 0;
-      int incl = val;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        int n = __shfl_up_sync(0xffffffffu, incl, o);
-        if ((int)threadIdx.x >= o) incl += n;
-      }
-      if (i < k) off[i] = carry + incl - val;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < k; i += blockDim.x) {
-    counts[(int64_t)bh * k + i] = hist[i];
-    offsets[(int64_t)bh * k + i] = off[i];
-  }
-  __syncthreads();
-  if (threadIdx.x < 32) {  // one warp scatters in token order, 32 tokens at a time
-    const unsigned lane = threadIdx.x;
-    int32_t* p = perm + (int64_t)bh * S;
-    for (int base = 0; base < S; base += 32) {
-      int t = base + (int)lane;
-      bool act = t < S;
-      int zz = act ? z[t] : -1 - (int)lane;  // inactive lanes get unique keys
-      unsigned peers = __match_any_sync(0xffffffffu, zz);
-      int rank = __popc(peers & ((1u << lane) - 1u));
-      int pos = act ? off[zz] + rank : 0;
-      __syncwarp();
-      if (act) {
-        p[pos] = t;
-        if (rank == 0) off[zz] += __popc(peers);
-      }
-      __syncwarp();
-    }
-  }
-}
-
-// Member means, one CTA per (cluster, batch-head); fp64 column sums over the cluster's tokens.
-__global__ void kmeans_update_kernel(const uint16_t* __restrict__ v, int S, int D, int k,
-                                     const int32_t* __restrict__ perm, const int32_t* __restrict__ counts,
-                                     const int32_t* __restrict__ offsets, float* __restrict__ cent,
-                                     float* __restrict__ cnorm) {
-  const int i = blockIdx.x, bh = blockIdx.y;
-  const int n = counts[(int64_t)bh * k + i];
-  const int o = offsets[(int64_t)bh * k + i];
-  const uint16_t* vh = v + (int64_t)bh * S * D;
-  const int32_t* ph = perm + (int64_t)bh * S;
-  float* c = cent + ((int64_t)bh * k + i) * D;
-  __shared__ float red[32];
-  float nrm = 0.f;
-  if (n > 0) {
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
-      double s = 0.0;
-      for (int m = 0; m < n; ++m) s += (double)bf16_bits_to_f32(vh[(int64_t)ph[o + m] * D + d]);
-      float cv = (float)(s / (double)n);
-      c[d] = cv;
-      nrm = fmaf(cv, cv, nrm);
-    }
-  } else {
-    for (int d = threadIdx.x; d < D; d += blockDim.x) nrm = fmaf(c[d], c[d], nrm);
-  }
-  for (int off = 16; off; off >>= 1) nrm += __shfl_xor_sync(0xffffffffu, nrm, off);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = nrm;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float s = 0.f;
-    for (int w = 0; w < (int)(blockDim.x + 31) / 32; ++w) s += red[w];
-    cnorm[(int64_t)bh * k + i] = s;
-  }
-}
-
 __global__ void iota_kernel(int32_t* __restrict__ perm, int S, int64_t total) {
   int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i < total) perm[i] = (int32_t)(i % S);
@@ -444,25 +240,8 @@ int prepare_launch(const PlanBuffers& p, const uint16_t* Q, const uint16_t* K, c
           cudaSuccess)
         return VC_ERR_CUDA;
     } else {
-      static bool attr_set = false;
-      if (!attr_set) {
-        if (cudaFuncSetAttribute(kmeans_assign_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kmeans_assign_smem<128>()) != cudaSuccess ||
-            cudaFuncSetAttribute(kmeans_assign_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kmeans_assign_smem<64>()) != cudaSuccess)
-          return VC_ERR_CUDA;
-        attr_set = true;
-      }
-      kmeans_init_kernel<<<dim3(k, BH), 128, 0, st>>>(V, S, D, k, p.cent, p.cnorm);
-      for (int it = 0; it < iters; ++it) {
-        dim3 ga((S + 63) / 64, BH);
-        if (D == 128)
-          kmeans_assign_kernel<128><<<ga, 256, kmeans_assign_smem<128>(), st>>>(V, S, k, p.cent, p.cnorm, p.labels);
-        else
-          kmeans_assign_kernel<64><<<ga, 256, kmeans_assign_smem<64>(), st>>>(V, S, k, p.cent, p.cnorm, p.labels);
-        argsort_kernel<<<BH, 1024, 0, st>>>(p.labels, S, k, p.perm, p.counts, p.offsets);
-        kmeans_update_kernel<<<dim3(k, BH), 128, 0, st>>>(V, S, D, k, p.perm, p.counts, p.offsets, p.cent, p.cnorm);
-      }
+      int rc = kmeans_launch(p, V, iters, st);
+      if (rc != VC_OK) return rc;
     }
     perm = p.perm;
   } else {

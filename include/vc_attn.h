@@ -22,7 +22,7 @@
  *     error the outputs are unspecified and the plan (if any) is left usable or destroyed as
  *     stated per call.
  *   - Supported shapes: D in {64, 128}; 1 <= S <= 1048576; B*H >= 1; B*H*ceil(S/128)*128*D below
- *     2^40 bytes; 1 <= k_clusters <= min(S, 1024); 0 <= iters <= 64.
+ *     2^40 bytes; 1 <= k_clusters <= min(S, 1024); 1 <= iters <= 64 whenever k-means runs.
  *   - No CPU fallback: every step of the computation runs in this library's CUDA kernels.
  */
 #ifndef VC_ATTN_H
@@ -82,8 +82,8 @@ typedef struct vc_plan vc_plan;
  *   Q and K' quantised to E4M3 with one scale per 128-token block (scale = absmax/448);
  *   mu_j = mean of the valid rows of block j of V', stored as bf16; R = V' - mu_j quantised to
  *   E4M3 with one scale per head (absmax/448), stored transposed and padded.
- * Q, K, V: device bf16 [B, H, S, D].  k_clusters, iters: k-means size and rounds (iters = 0
- * keeps the initial assignment of the first round).  *plan: NULL to allocate a new plan, or an
+ * Q, K, V: device bf16 [B, H, S, D].  k_clusters, iters: k-means size and rounds
+ * (1 <= iters <= 64, else VC_ERR_INVALID_ARG; each round = assignment, argsort, centroid update).  *plan: NULL to allocate a new plan, or an
  * existing plan of the same (B, H, S, D, k_clusters), whose buffers are reused without any
  * allocation (VC_ERR_PLAN_MISMATCH if the shape differs; the plan is left untouched).
  * The first call allocates device memory (synchronous cudaMalloc); later calls reusing the plan
@@ -132,7 +132,11 @@ size_t vc_plan_size(const vc_plan* plan, int what);
 /* Enqueue a copy of one plan tensor into dst (host or device memory, `bytes` >= its size). */
 int vc_plan_get(const vc_plan* plan, int what, void* dst, size_t bytes, cudaStream_t stream);
 /* Synchronise `stream`, read and clear the plan's device status word. Returns VC_OK, or
- * VC_ERR_TIMEOUT if a kernel recorded a timeout since the last call (bits in *bits if non-NULL). */
+ * VC_ERR_TIMEOUT if a kernel recorded a timeout since the last call (bits in *bits if non-NULL).
+ * Every wait inside the kernels is bounded; a wait that runs out sets a bit and the kernel
+ * returns without touching its outputs further:
+ *   1 forward: score tile wait      2 forward: P / S-buffer hand-off   4 forward: a TMA load
+ *   8 forward: PV completion       16 forward: teardown drain         32 k-means assignment */
 int vc_plan_status(vc_plan* plan, cudaStream_t stream, int* bits);
 /* Shape of a plan; any output pointer may be NULL. */
 int vc_plan_shape(const vc_plan* plan, int* B, int* H, int* S, int* D, int* k_clusters);
