@@ -10,8 +10,8 @@
 // GB300 design (not the pages' kernel): one CTA per 128-row query tile and batch-head.
 //   producer    TMA: Q once; K' and V^T tiles of 128 keys into 3-stage rings; with
 //               V-Smooth, the transposed bf16 means of each 16-tile block run into a 2-stage ring.
-//   MMA issuer  one thread: S = Q K'^T (kind::f8f6f4, SS) into one of two TMEM score
-//               buffers; O += P V and W += P E_{j mod 16} (TS: the codes P are read from TMEM),
+//   MMA issuer  one warp, one elected lane issuing: S = Q K'^T for two key tiles at once
+//               (kind::f8f6f4, SS, N = 256) into the two TMEM score buffers; O += P V and W += P E_{j mod 16} (TS: the codes P are read from TMEM),
 //               where E_s is a one-hot 16 x 128 block, so column j mod 16 of W receives the exact
 //               row sum of tile j; at the end of each run of tiles from one 16-tile block, the
 //               mean term O += F M^T (kind::f16, F = W / sV split into bf16 hi + lo, M the block's
@@ -39,7 +39,7 @@ constexpr float kFastMaxAbsM = 1048576.f;  // |M| below 2^20 code units: the one
 
 template <int D>
 struct FwdCfg {
-  static constexpr int NKP = 2, NV = 3, NMU = 2;
+  static constexpr int NKP = 2, NV = 4, NMU = 2;
   static constexpr int QB = 128 * D;             // bytes of a Q or K tile (128 rows x D codes)
   static constexpr int KPB = 2 * QB;             // a K stage: the two key tiles of one S pair
   static constexpr int VB = D * 128;             // bytes of a V^T tile (D rows x 128 keys)
@@ -52,11 +52,15 @@ struct FwdCfg {
   static constexpr int OFF_V = OFF_K + NKP * KPB;
   static constexpr int OFF_MU = OFF_V + NV * VSTAGE;
   static constexpr int OFF_BAR = OFF_MU + NMU * MUB;
-  static constexpr int NBAR = 1 + 2 * NKP + 2 * NV + 2 * NMU + 1 + 1 + 2 + 4 + 1 + 1;
+  static constexpr int NBAR = 1 + 2 * NKP + NV + 2 * NMU + 1 + 1 + 2 + 4 + 1 + 1 + 8;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int OFF_MBUF = OFF_MISC + 64;    // running max hand-off, 2 x 128 floats
-  static constexpr int OFF_MSEQ = OFF_MBUF + 1024;  // 4 publication counters
-  static constexpr int SMEM = OFF_MSEQ + 64 + 1024; // + slack for aligning the base to 1024
+  static constexpr int OFF_MBUF = OFF_MISC + 64;       // running max hand-off, 2 x 128 floats
+  static constexpr int SMEM = OFF_MBUF + 1024 + 1024;  // + slack for aligning the base to 1024
+  static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
+  static_assert(OFF_V % 1024 == 0 && VSTAGE % 1024 == 0 && OFF_K % 1024 == 0, "128-byte swizzle atoms");
+  // A V stage is refilled once PV of its previous tile is complete (o_done): with at most four
+  // stages PV(t + 4) needs the tile being loaded, so that barrier cannot run two phases ahead.
+  static_assert(NV <= 4, "V stages are released through o_done[t & 3]");
   // TMEM columns: O|W [0, D+16), F [D+16, D+32), l [D+32], P0 [176, 208), P1 [208, 240),
   // S pair [256, 512): the scores of tile 2k in [256, 384), of tile 2k+1 in [384, 512).
   static constexpr uint32_t T_O = 0, T_W = D, T_F = D + 16, T_L = D + 32, T_P0 = 176, T_P1 = 208, T_S = 256;
@@ -199,8 +203,7 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
   uint64_t* k_full = q_full + 1;          // per K pair stage
   uint64_t* k_empty = k_full + C::NKP;
   uint64_t* v_full = k_empty + C::NKP;
-  uint64_t* v_empty = v_full + C::NV;
-  uint64_t* mu_full = v_empty + C::NV;
+  uint64_t* mu_full = v_full + C::NV;
   uint64_t* mu_empty = mu_full + C::NMU;
   uint64_t* s_full = mu_empty + C::NMU;   // S pair k landed (one phase per pair)
   uint64_t* s_free = s_full + 1;          // both groups hold S pair k in registers (256 arrivals)
@@ -212,10 +215,12 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
   uint64_t* o_done = p_full + 2;
   uint64_t* f_full = o_done + 4;
   uint64_t* drain = f_full + 1;
+  // mx_full[slot][quarter]: the 32 running maxima of one row quarter after position t, slot t & 1,
+  // published by the group that owns t (32 arrivals, each after its own mbuf store).
+  uint64_t* mx_full = drain + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base + C::OFF_MISC + 8);
   float* mbuf = reinterpret_cast<float*>(base + C::OFF_MBUF);
-  int* mseq = reinterpret_cast<int*>(base + C::OFF_MSEQ);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qt = blockIdx.x, bh = blockIdx.y;
@@ -227,7 +232,7 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
   if (tid == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < C::NKP; ++s) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
-    for (int s = 0; s < C::NV; ++s) { mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1); }
+    for (int s = 0; s < C::NV; ++s) mbar_init(&v_full[s], 1);
     for (int s = 0; s < C::NMU; ++s) { mbar_init(&mu_full[s], 1); mbar_init(&mu_empty[s], 1); }
     mbar_init(s_full, 1);
     mbar_init(s_free, 256);
@@ -237,7 +242,7 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
     mbar_init(f_full, 128);
     mbar_init(drain, 1);
     *abort_flag = 0;
-    for (int i = 0; i < 4; ++i) mseq[i] = 0;
+    for (int i = 0; i < 8; ++i) mbar_init(&mx_full[i], 32);
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(tmem_slot, 512);
@@ -311,7 +316,7 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
         break;
       }
       const int sv = t % C::NV;
-      if (!leader_wait(&v_empty[sv], ((t / C::NV) & 1) ^ 1)) { loads_ok = false; break; }
+      if (t >= C::NV && !leader_wait(&o_done[(t - C::NV) & 3], ((t - C::NV) >> 2) & 1)) { loads_ok = false; break; }
       {  // one-hot rows: a constant row is invariant under the 16-byte chunk swizzle
         uint4* onehot = reinterpret_cast<uint4*>(sV + sv * C::VSTAGE + C::VB);
 #pragma unroll
@@ -341,101 +346,115 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------------ MMA issuer
+    // The whole warp runs the schedule, so its loop state stays warp-uniform; one elected lane
+    // issues every MMA group and commit (a commit tracks the MMAs of the thread that issues it).
     // Per pair k: once both groups hold S pair k in registers, S pair k+1 = Q K'(2k+2, 2k+3)^T as
     // one N = 256 MMA group; then per tile t of the pair, the mean term of a finished block run and
     // O|W += P(t) [V(t); E_{j mod 16}] as one N = D+16 MMA group.
-    if (lane == 0) {
-      const uint32_t tO = tmem + C::T_O, tF = tmem + C::T_F, tS = tmem + C::T_S;
-      const uint32_t tP0 = tmem + C::T_P0, tP1 = tmem + C::T_P1;
-      constexpr uint32_t id_qk = idesc_e4m3(128, 256), id_pv = idesc_e4m3(128, D + 16);
-      constexpr uint32_t id_mu = idesc_bf16(128, D);
-      // Descriptors are built once; a stage or K step only adds to the start-address field
-      // (addresses are below 2^18, so the 14-bit field never carries).
-      const uint64_t dq = smem_desc(sQ, C::QK_SBO, C::QK_LAYOUT);
-      const uint64_t dk0 = smem_desc(sK, C::QK_SBO, C::QK_LAYOUT);
-      const uint64_t dv0 = smem_desc(sV, 1024, kSw128);
-      const uint64_t dmu0 = smem_desc(sMu, 256, kSw32);
-      auto issue_qk = [&](int k) -> bool {
-        const int s = k % C::NKP;
-        if (!wait_or_abort(&k_full[s], (k / C::NKP) & 1, kWaitLimit, abort_flag)) return false;
-        tc_fence_after();
+    const bool leader = elect_one();
+    const uint32_t tO = tmem + C::T_O, tF = tmem + C::T_F, tS = tmem + C::T_S;
+    const uint32_t tP0 = tmem + C::T_P0, tP1 = tmem + C::T_P1;
+    constexpr uint32_t id_qk = idesc_e4m3(128, 256), id_pv = idesc_e4m3(128, D + 16);
+    constexpr uint32_t id_mu = idesc_bf16(128, D);
+    // Descriptors are built once; a stage or K step only adds to the start-address field
+    // (addresses are below 2^18, so the 14-bit field never carries).
+    const uint64_t dq = smem_desc(sQ, C::QK_SBO, C::QK_LAYOUT);
+    const uint64_t dk0 = smem_desc(sK, C::QK_SBO, C::QK_LAYOUT);
+    const uint64_t dv0 = smem_desc(sV, 1024, kSw128);
+    const uint64_t dmu0 = smem_desc(sMu, 256, kSw32);
+    auto fail = [&](int bit) {
+      if (lane == 0) record_failure(args.status, abort_flag, bit);
+    };
+    auto issue_qk = [&](int k) -> bool {
+      const int s = k % C::NKP;
+      if (!warp_wait(&k_full[s], (k / C::NKP) & 1, kWaitLimit, abort_flag)) return false;
+      tc_fence_after();
+      if (leader) {
         const uint64_t dk = dk0 + (uint64_t)(s * (C::KPB >> 4));
 #pragma unroll
         for (int kk = 0; kk < D / 32; ++kk) mma_e4m3_ss(tS, dq + 2 * kk, dk + 2 * kk, id_qk, kk > 0);
         mma_commit(s_full);
         mma_commit(&k_empty[s]);
-        return true;
-      };
-      // O += F M^T for the block run with ordinal q: two K=16 bf16 MMAs, hi then lo.
-      auto issue_mean = [&](int q) -> bool {
-        const int sm = q % C::NMU;
-        if (!wait_or_abort(&mu_full[sm], (q / C::NMU) & 1, kWaitLimit, abort_flag)) return false;
-        tc_fence_after();
+      }
+      __syncwarp();
+      return true;
+    };
+    // O += F M^T for the block run with ordinal q: two K=16 bf16 MMAs, hi then lo.
+    auto issue_mean = [&](int q) -> bool {
+      const int sm = q % C::NMU;
+      if (!warp_wait(&mu_full[sm], (q / C::NMU) & 1, kWaitLimit, abort_flag)) return false;
+      tc_fence_after();
+      if (leader) {
         const uint64_t bdesc = dmu0 + (uint64_t)(sm * (C::MUB >> 4));
         mma_bf16_ts(tO, tF, bdesc, id_mu, 1);
         mma_bf16_ts(tO, tF + 8, bdesc, id_mu, 1);
         mma_commit(&mu_empty[sm]);
-        return true;
-      };
-      bool ok = mbar_wait(q_full, 0, kWaitLimit) && issue_qk(0);
-      if (!ok) record_failure(args.status, abort_flag, kStatusTimeoutLoad);
-      int seg = -1;  // ordinal of the current block run
-      for (int k = 0; ok && k < npairs; ++k) {
-        if (*abort_flag) { ok = false; break; }
-        if (k + 1 < npairs) {
-          if (!wait_or_abort(s_free, k & 1, kWaitLimit, abort_flag)) {
-            record_failure(args.status, abort_flag, kStatusTimeoutP);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          if (!issue_qk(k + 1)) {
-            record_failure(args.status, abort_flag, kStatusTimeoutLoad);
-            ok = false;
-            break;
-          }
+      }
+      __syncwarp();
+      return true;
+    };
+    bool ok = warp_wait(q_full, 0, kWaitLimit, abort_flag) && issue_qk(0);
+    if (!ok) fail(kStatusTimeoutLoad);
+    int seg = -1;  // ordinal of the current block run
+    for (int k = 0; ok && k < npairs; ++k) {
+      if (k + 1 < npairs) {
+        if (!warp_wait(s_free, k & 1, kWaitLimit, abort_flag)) {
+          fail(kStatusTimeoutP);
+          ok = false;
+          break;
         }
-        for (int t = 2 * k; ok && t <= 2 * k + 1 && t < nkb; ++t) {
-          const int g = t & 1;
-          if (!wait_or_abort(&p_full[g], k & 1, kWaitLimit, abort_flag)) {
-            record_failure(args.status, abort_flag, kStatusTimeoutP);
+        tc_fence_after();
+        if (!issue_qk(k + 1)) {
+          fail(kStatusTimeoutLoad);
+          ok = false;
+          break;
+        }
+      }
+      for (int t = 2 * k; t <= 2 * k + 1 && t < nkb; ++t) {
+        const int g = t & 1;
+        if (!warp_wait(&p_full[g], k & 1, kWaitLimit, abort_flag)) {
+          fail(kStatusTimeoutP);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (seg_start(t, start)) {
+          if (use_mean && seg >= 0 && !issue_mean(seg)) {
+            fail(kStatusTimeoutLoad);
             ok = false;
             break;
           }
-          tc_fence_after();
-          if (seg_start(t, start)) {
-            if (use_mean && seg >= 0 && !issue_mean(seg)) {
-              record_failure(args.status, abort_flag, kStatusTimeoutLoad);
-              ok = false;
-              break;
-            }
-            ++seg;
-          }
-          const int sv = t % C::NV;
-          if (!wait_or_abort(&v_full[sv], (t / C::NV) & 1, kWaitLimit, abort_flag)) {
-            record_failure(args.status, abort_flag, kStatusTimeoutLoad);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+          ++seg;
+        }
+        const int sv = t % C::NV;
+        if (!warp_wait(&v_full[sv], (t / C::NV) & 1, kWaitLimit, abort_flag)) {
+          fail(kStatusTimeoutLoad);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (leader) {
           const uint32_t tP = g ? tP1 : tP0;
           const uint64_t dv = dv0 + (uint64_t)(sv * (C::VSTAGE >> 4));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) mma_e4m3_ts(tO, tP + 8 * kk, dv + 2 * kk, id_pv, (t > 0 || kk > 0));
-          mma_commit(&o_done[t & 3]);
-          mma_commit(&v_empty[sv]);
+          mma_commit(&o_done[t & 3]);  // also releases V stage t % NV to the V producer
         }
+        __syncwarp();
       }
-      if (ok && use_mean && !*abort_flag) {  // the last block run: its F arrives after the loop
-        if (!wait_or_abort(f_full, 0, kWaitLimit, abort_flag) || !issue_mean(seg))
-          record_failure(args.status, abort_flag, kStatusTimeoutP);
-        else
-          mma_commit(&o_done[nkb & 3]);  // as if it were tile nkb
-      }
-      // Teardown: every MMA this thread issued has completed before TMEM is released.
-      mma_commit(drain);
-      if (!mbar_wait(drain, 0, kWaitLimit)) record_failure(args.status, abort_flag, kStatusTimeoutDrain);
     }
+    if (ok && use_mean && !warp_aborted(abort_flag)) {  // the last block run: its F arrives after the loop
+      if (!warp_wait(f_full, 0, kWaitLimit, abort_flag) || !issue_mean(seg)) {
+        fail(kStatusTimeoutP);
+      } else {
+        if (leader) mma_commit(&o_done[nkb & 3]);  // as if it were tile nkb
+        __syncwarp();
+      }
+    }
+    // Teardown: every MMA this warp issued has completed before TMEM is released.
+    if (leader) mma_commit(drain);
+    __syncwarp();
+    if (!__all_sync(0xffffffffu, mbar_wait(drain, 0, kWaitLimit))) fail(kStatusTimeoutDrain);
   } else if (warp < 8) {
     // ------------------------------------------------------------------ softmax warps 0-7
     // Group g takes tile t = 2k + g of every S pair k, one thread per query row, its 128 scores
@@ -483,19 +502,10 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
 #pragma unroll
       for (int s = 0; s < 16; ++s) w[s] = __uint_as_float(wr[s]);
     };
-    // Wait (bounded) until the running max after position t-1 has been published.
+    // Wait (bounded) until the running max after position t-1 has been published. A slot's phase
+    // cannot run ahead: position t+1 is published only after this group has published t.
     auto wait_max = [&](int t) -> bool {
-      bool got = true;
-      if (lane == 0) {
-        got = false;
-        for (uint32_t i = 0; i < (kWaitLimit << 6); ++i) {
-          if (ld_acquire_cta(&mseq[wq]) >= t) { got = true; break; }
-          if ((i & 255u) == 255u && *abort_flag) break;
-        }
-      }
-      got = __shfl_sync(0xffffffffu, got, 0);
-      __syncwarp();
-      return got;
+      return warp_wait(&mx_full[((t - 1) & 1) * 4 + wq], ((t - 1) >> 1) & 1, kWaitLimit, abort_flag);
     };
 
     if (wg == 0) {  // l starts at 0
@@ -558,8 +568,7 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
       const float Mn = fmaxf(M, tmax);
       if (t + 1 < nkb) {  // hand the running max to the other group as early as possible
         mbuf[(t & 1) * 128 + row] = Mn;
-        __syncwarp();
-        if (lane == 0) st_release_cta(&mseq[wq], t + 1);
+        mbar_arrive(&mx_full[(t & 1) * 4 + wq]);  // release: orders this lane's store before the arrival
       }
       // Codes. P(t) reuses the columns of P(t-2), which PV(t-2) must have read.
       if (!ensure_pv(t - 2)) { ok = false; break; }

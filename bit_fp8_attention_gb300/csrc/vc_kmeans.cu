@@ -117,7 +117,7 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d, uint64_t a, uint64_t b, 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   for (uint32_t i = 0; i < kWaitLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 255u && *abort_flag) return false;
+    if ((i & 15u) == 15u && *abort_flag) return false;
   }
   return false;
 }

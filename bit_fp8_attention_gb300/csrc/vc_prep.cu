@@ -227,7 +227,7 @@ static int check_launch() { return cudaPeekAtLastError() == cudaSuccess ? 0 : VC
 
 int prepare_launch(const PlanBuffers& p, const uint16_t* Q, const uint16_t* K, const uint16_t* V,
                    const int32_t* perm_in, bool vsmooth, int iters, cudaStream_t st) {
-  const int BH = p.B * p.H, S = p.S, D = p.D, k = p.k, nkb = p.nkb, S_pad = p.S_pad;
+  const int BH = p.B * p.H, S = p.S, D = p.D, nkb = p.nkb, S_pad = p.S_pad;
   dim3 gblk(nkb, BH);
   // Q: per-block quantisation in token order
   if (D == 128) quant_blocks_kernel<128><<<gblk, 256, 0, st>>>(Q, nullptr, S, S_pad, p.qcodes, p.qscales);
