@@ -17,8 +17,9 @@
 //               mean term O += F M^T (kind::f16, F = W / sV split into bf16 hi + lo, M the block's
 //               16 means) -- Eq. 6's r mu^T for 16 tiles at once, in the same accumulator.
 //   warps 0-7   softmax, two warpgroups on alternate key tiles, one thread per query row: tile max
-//               on the raw scores, true-score max in code units handed between the groups, O/W/l
-//               rescale on every increase, E4M3 codes written into TMEM.
+//               on the raw scores, handed to the other group as soon as it is known; each group
+//               keeps the running max (code units) by folding in the other group's tile maxima;
+//               O/W/l rescale on every increase, E4M3 codes written into TMEM.
 //   warp 8      TMA producer of Q and the K pairs; warp 10 TMA producer of V (with the one-hot rows)
 //               and the mean blocks; warp 9 MMA issuer.
 // TMEM columns: O [0, D), W [D, D+16), F [D+16, D+32), l [D+32], P [176, 208) and [208, 240),
@@ -52,10 +53,10 @@ struct FwdCfg {
   static constexpr int OFF_V = OFF_K + NKP * KPB;
   static constexpr int OFF_MU = OFF_V + NV * VSTAGE;
   static constexpr int OFF_BAR = OFF_MU + NMU * MUB;
-  static constexpr int NBAR = 1 + 2 * NKP + NV + 2 * NMU + 1 + 1 + 2 + 4 + 1 + 1 + 8;
+  static constexpr int NBAR = 1 + 2 * NKP + NV + 2 * NMU + 1 + 1 + 2 + 4 + 1 + 1 + 32;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int OFF_MBUF = OFF_MISC + 64;       // running max hand-off, 2 x 128 floats
-  static constexpr int SMEM = OFF_MBUF + 1024 + 1024;  // + slack for aligning the base to 1024
+  static constexpr int OFF_MBUF = OFF_MISC + 64;       // tile maxima hand-off, 8 slots x 128 floats
+  static constexpr int SMEM = OFF_MBUF + 4096 + 1024;  // + slack for aligning the base to 1024
   static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
   static_assert(OFF_V % 1024 == 0 && VSTAGE % 1024 == 0 && OFF_K % 1024 == 0, "128-byte swizzle atoms");
   // A V stage is refilled once PV of its previous tile is complete (o_done): with at most four
@@ -215,8 +216,10 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
   uint64_t* o_done = p_full + 2;
   uint64_t* f_full = o_done + 4;
   uint64_t* drain = f_full + 1;
-  // mx_full[slot][quarter]: the 32 running maxima of one row quarter after position t, slot t & 1,
-  // published by the group that owns t (32 arrivals, each after its own mbuf store).
+  // mx_full[slot][quarter]: the 32 raw-score tile maxima (code units) of one row quarter for
+  // position t, slot t & 7, published by the group that owns t (32 arrivals, each after its own
+  // mbuf store). Slot t & 7 is rewritten at t+8, whose scores exist only after the other group has
+  // loaded position t+5 or later, i.e. after it has finished t+1, where it read the slot.
   uint64_t* mx_full = drain + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base + C::OFF_MISC + 8);
@@ -242,7 +245,7 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
     mbar_init(f_full, 128);
     mbar_init(drain, 1);
     *abort_flag = 0;
-    for (int i = 0; i < 8; ++i) mbar_init(&mx_full[i], 32);
+    for (int i = 0; i < 32; ++i) mbar_init(&mx_full[i], 32);
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(tmem_slot, 512);
@@ -502,11 +505,11 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
 #pragma unroll
       for (int s = 0; s < 16; ++s) w[s] = __uint_as_float(wr[s]);
     };
-    // Wait (bounded) until the running max after position t-1 has been published. A slot's phase
-    // cannot run ahead: position t+1 is published only after this group has published t.
-    auto wait_max = [&](int t) -> bool {
-      return warp_wait(&mx_full[((t - 1) & 1) * 4 + wq], ((t - 1) >> 1) & 1, kWaitLimit, abort_flag);
+    // Wait (bounded) until the tile max of position t-1 has been published (see mx_full).
+    auto wait_tmax = [&](int t) -> bool {
+      return warp_wait(&mx_full[((t - 1) & 7) * 4 + wq], ((t - 1) >> 3) & 1, kWaitLimit, abort_flag);
     };
+    float Mrun = -INFINITY;  // this group's copy of the running max, after its previous tile
 
     if (wg == 0) {  // l starts at 0
       tmem_st1(tL, 0u);
@@ -556,20 +559,23 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
       const float mx = fmaxf(max3f(m8[0], m8[1], m8[2]), max3f(max3f(m8[3], m8[4], m8[5]), m8[6], m8[7]));
       const float aj = aq * sk;
       const float tmax = mx * aj;  // = max_c fl(s_c * a_j): rounding is monotone and a_j > 0
+      if (t + 1 < nkb) {  // the tile max goes to the other group at once; it depends on nothing else
+        mbuf[(t & 7) * 128 + row] = tmax;
+        mbar_arrive(&mx_full[(t & 7) * 4 + wq]);  // release: orders this lane's store before the arrival
+      }
+      // M(t-1) = max(M(t-2), tmax(t-1)): this group's running max after its previous tile, with the
+      // other group's tile in between folded in.
       float M = -INFINITY;
       if (t > 0) {
-        if (!wait_max(t)) {
+        if (!wait_tmax(t)) {
           record_failure(args.status, abort_flag, kStatusTimeoutS);
           ok = false;
           break;
         }
-        M = mbuf[((t - 1) & 1) * 128 + row];
+        M = fmaxf(Mrun, mbuf[((t - 1) & 7) * 128 + row]);
       }
       const float Mn = fmaxf(M, tmax);
-      if (t + 1 < nkb) {  // hand the running max to the other group as early as possible
-        mbuf[(t & 1) * 128 + row] = Mn;
-        mbar_arrive(&mx_full[(t & 1) * 4 + wq]);  // release: orders this lane's store before the arrival
-      }
+      Mrun = Mn;
       // Codes. P(t) reuses the columns of P(t-2), which PV(t-2) must have read.
       if (!ensure_pv(t - 2)) { ok = false; break; }
       const float bb = __fsub_rn(kB0, Mn);
