@@ -12,7 +12,9 @@ amortised over the grouping schedule of the pages (a 40-step run regroups at ste
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
+import re
 import math
 import os
 import statistics
@@ -57,6 +59,34 @@ def dist_env():
 def workload_name(cfg):
     return (f"{cfg['name']}: B={cfg['B']} H={cfg['H']} S={cfg['S']} D={cfg['D']} "
             f"grid={'x'.join(map(str, cfg['grid']))} k={cfg['k']} iters={cfg['iters']}")
+
+
+FWD_SOURCES = ("vc_fwd.cu", "vc_device.cuh", "vc_internal.h")
+
+
+def forward_source_hash() -> str:
+    """First 16 hex digits of the sha256 of the forward kernel's sources (which ncu counters are valid for)."""
+    h = hashlib.sha256()
+    for name in FWD_SOURCES:
+        with open(os.path.join(ROOT, "bit_fp8_attention_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(cfg):
+    """DRAM bytes (read + write) per forward launch from the committed ncu summary of this workload, or None
+    when there is none or it was taken on other forward sources than the ones built now."""
+    path = os.path.join(ROOT, "profiles", f"vc_fwd_kernel_{cfg['name']}_d{cfg['D']}_s{cfg['S']}_dram.md")
+    try:
+        with open(path) as f:
+            text = f.read()
+    except OSError:
+        return None
+    m_hash = re.search(r"forward source sha256/16: `?([0-9a-f]{16})", text)
+    m_bytes = re.search(r"traffic per launch: (\d+) bytes", text)
+    if not (m_hash and m_bytes) or m_hash.group(1) != forward_source_hash():
+        return None
+    return int(m_bytes.group(1))
 
 
 def measured_peaks():
@@ -321,7 +351,7 @@ def main():
         "prepare_ms": t_prep_full, "prepare_quant_ms": t_prep_quant, "grouping_ms": t_group,
         "amortised_prepare_ms": t_prep_quant + 3.0 / 40.0 * t_group,
         "roofline": {"bound": "tensor", "kernel": "vc_fwd_kernel<128>", "achieved": fwd_tflops, "peak": fp8_peak,
-                     "unit": "TFLOP/s", "frac": fwd_tflops / fp8_peak, "traffic": None,
+                     "unit": "TFLOP/s", "frac": fwd_tflops / fp8_peak, "traffic": profiled_traffic(cfg),
                      "peak_source": f"{src} bf16 burst {bf16_burst:.0f} TFLOP/s x {FP8_OVER_BF16:.0f} (FP8/BF16 nominal)"},
         "clocks": clocks, "gpu_launches": launches_per_step(cfg) * args.steps,
     }
