@@ -36,7 +36,9 @@ namespace vc {
 
 constexpr uint32_t kWaitLimit = 1u << 20;
 constexpr float kB0 = 119.65f;             // 8*8 + 56 + beta, beta = -0.35
-constexpr float kFastMaxAbsM = 1048576.f;  // |M| below 2^20 code units: the one-FMA code is <= 120
+// Below 2^22 code units, |M| keeps y = fma(s, a, 119.65 - M) under 120.5: the rounding of s * a to the
+// running max and of b each add at most half an ulp of M (<= 0.25), so no code needs the clip at 120.
+constexpr float kClampFreeMaxAbsM = 4194304.f;
 
 template <int D>
 struct FwdCfg {
@@ -96,8 +98,9 @@ __device__ __forceinline__ uint64_t pack2f(float lo, float hi) {
 //   i.e. y to the nearest integer with ties to even, and the float's bit pattern is that integer
 //   with y's sign (FMUL2);
 //   cvt.pack.sat.u8 reads the patterns as s32, so negative codes clamp to 0, and packs them.
-// Equals clip[0,120](rne(fmaf(s, a, b))) whenever y < 120.5; the forward only calls it when the
-// running max keeps y below that (|M| < 2^20), and the single-score export clamps at 120 after it.
+// Equals clip[0,120](rne(fmaf(s, a, b))) whenever y < 120.5. Above that the code bytes only need a
+// byte-wise min with 120 (y >= 2^23 leaves the subnormal range and saturates to 255 first), which
+// the forward applies when |M| >= 2^22 and the single-score export always applies.
 __device__ __forceinline__ uint32_t expcast4(float s0, float s1, float s2, float s3, uint64_t a01, uint64_t a23,
                                              uint64_t b01, uint64_t b23) {
   const uint64_t tiny2 = (1ull << 32) | 1ull;  // (2^-149, 2^-149)
@@ -116,12 +119,6 @@ __device__ __forceinline__ uint32_t expcast4(float s0, float s1, float s2, float
   return d;
 }
 
-// Reference form of one code, used when |M| is too large for the fast path.
-__device__ __forceinline__ uint32_t expcast_code(float s, float a, float b) {
-  float r = rintf(__fmaf_rn(s, a, b));
-  r = fminf(fmaxf(r, 0.f), 120.f);
-  return (uint32_t)r;
-}
 // The conventional path: exponentiate in fp32, then a rounding E4M3 cast.
 __device__ __forceinline__ uint32_t expcast_off_code(float s, float a, float b) {
   float y = __fmaf_rn(s, a, b);
@@ -190,7 +187,7 @@ __device__ __forceinline__ void store_flush_operand(uint32_t tF, const float (&w
   tmem_st16(tF, f);
 }
 
-template <int D>
+template <int D, bool kExpCast>
 __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ FwdMaps maps, const FwdArgs args) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -476,7 +473,6 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
     const float aq = args.code_scale * args.qscales[(int64_t)bh * nkb + qt];
     const float sv = args.vscales[bh];
     const float inv_sv = 1.f / sv;
-    const bool expcast = (args.flags & VC_EXPCAST) != 0;
     const int tail_valid = args.S - (nkb - 1) * 128;
     bool ok = true;
     int known = -1;  // every PV up to this tile is known complete
@@ -579,33 +575,43 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
       // Codes. P(t) reuses the columns of P(t-2), which PV(t-2) must have read.
       if (!ensure_pv(t - 2)) { ok = false; break; }
       const float bb = __fsub_rn(kB0, Mn);
-      const bool fast = expcast && __all_sync(0xffffffffu, fabsf(Mn) < kFastMaxAbsM);
       const uint64_t a2 = pack2f(aj, aj), b2 = pack2f(bb, bb);
+      if constexpr (kExpCast) {
+        if (__all_sync(0xffffffffu, fabsf(Mn) < kClampFreeMaxAbsM)) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[16];
-        if (fast) {
+          for (int h = 0; h < 2; ++h) {
+            uint32_t pk[16];
 #pragma unroll
-          for (int g = 0; g < 16; ++g) {
-            const int c = 64 * h + 4 * g;
-            pk[g] = expcast4(s[c], s[c + 1], s[c + 2], s[c + 3], a2, a2, b2, b2);
+            for (int g = 0; g < 16; ++g) {
+              const int c = 64 * h + 4 * g;
+              pk[g] = expcast4(s[c], s[c + 1], s[c + 2], s[c + 3], a2, a2, b2, b2);
+            }
+            tmem_st16(tP + 16 * h, pk);
           }
-        } else if (expcast) {
+        } else {  // a running max beyond 2^22 code units: clip the codes at 120 byte by byte
 #pragma unroll
-          for (int g = 0; g < 16; ++g) {
-            const int c = 64 * h + 4 * g;
-            pk[g] = pack4(expcast_code(s[c], aj, bb), expcast_code(s[c + 1], aj, bb), expcast_code(s[c + 2], aj, bb),
-                          expcast_code(s[c + 3], aj, bb));
+          for (int h = 0; h < 2; ++h) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int g = 0; g < 16; ++g) {
+              const int c = 64 * h + 4 * g;
+              pk[g] = __vminu4(expcast4(s[c], s[c + 1], s[c + 2], s[c + 3], a2, a2, b2, b2), 0x78787878u);
+            }
+            tmem_st16(tP + 16 * h, pk);
           }
-        } else {
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[16];
 #pragma unroll
           for (int g = 0; g < 16; ++g) {
             const int c = 64 * h + 4 * g;
             pk[g] = pack4(expcast_off_code(s[c], aj, bb), expcast_off_code(s[c + 1], aj, bb),
                           expcast_off_code(s[c + 2], aj, bb), expcast_off_code(s[c + 3], aj, bb));
           }
+          tmem_st16(tP + 16 * h, pk);
         }
-        tmem_st16(tP + 16 * h, pk);
       }
       // A new block run: the previous run's row sums (complete once PV(t-1) is done) leave W.
       // Every max increase rescales O, W and l by alpha = 2^((M - M')/8).
@@ -743,12 +749,13 @@ int encode_fwd_maps(const PlanBuffers& p, FwdMaps* maps) {
   return rc;
 }
 
-template <int D>
+template <int D, bool kExpCast>
 static int launch_fwd(const PlanBuffers& p, const FwdMaps& maps, uint16_t* O, unsigned flags, cudaStream_t st) {
   using C = FwdCfg<D>;
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(vc_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+    if (cudaFuncSetAttribute(vc_fwd_kernel<D, kExpCast>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+        cudaSuccess)
       return VC_ERR_CUDA;
     attr_set = true;
   }
@@ -765,12 +772,16 @@ static int launch_fwd(const PlanBuffers& p, const FwdMaps& maps, uint16_t* O, un
   a.code_scale = (float)(8.0 * 1.4426950408889634 / __builtin_sqrt((double)D));
   a.use_mean = (p.has_means && (flags & VC_VSMOOTH)) ? 1 : 0;
   dim3 grid(p.nkb, p.B * p.H);
-  vc_fwd_kernel<D><<<grid, 352, C::SMEM, st>>>(maps, a);
+  vc_fwd_kernel<D, kExpCast><<<grid, 352, C::SMEM, st>>>(maps, a);
   return cudaPeekAtLastError() == cudaSuccess ? VC_OK : VC_ERR_CUDA;
 }
 
 int forward_launch(const PlanBuffers& p, const FwdMaps& maps, uint16_t* O, unsigned flags, cudaStream_t st) {
-  return p.D == 128 ? launch_fwd<128>(p, maps, O, flags, st) : launch_fwd<64>(p, maps, O, flags, st);
+  // ExpCast on and off are separate instantiations, so the default kernel carries only its own code.
+  const bool ec = (flags & VC_EXPCAST) != 0;
+  if (p.D == 128)
+    return ec ? launch_fwd<128, true>(p, maps, O, flags, st) : launch_fwd<128, false>(p, maps, O, flags, st);
+  return ec ? launch_fwd<64, true>(p, maps, O, flags, st) : launch_fwd<64, false>(p, maps, O, flags, st);
 }
 
 int expcast_launch(const float* s, const float* a, const float* b, int64_t n, uint8_t* out, cudaStream_t st) {

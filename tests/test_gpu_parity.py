@@ -5,6 +5,8 @@ The forward follows "VC-Attention: Value Smoothing and Softmax Casting for Low-b
 argsort permutations bit-exact; O within rel-L2 1e-2 and max-abs 3e-2 max|V| per head against the
 quantised oracle fed the GPU's permutation; the k-means objective within 1% of the oracle's.
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -195,4 +197,28 @@ def test_repeated_launches_never_stall(m, D):
                 ref = O.clone()
             else:
                 assert torch.equal(ref.view(torch.int16), O.view(torch.int16)), f"flags {flags} launch {rep}"
+    plan.destroy()
+
+
+def test_huge_scores_take_the_clamped_code_path(m):
+    """Row maxima far beyond 2^22 code units: the forward's byte-wise clip at 120 ("VC-Attention", Sec. 3.3
+    Eq. 7) is exercised. Q = K = +-224 per element, so every row's own key scores 224^2 * sqrt(128) ~ 5.7e5,
+    i.e. ~6.5e6 code units, while every other key scores far lower: P is one-hot and O is close to V of the
+    row's own token."""
+    S, D, H = 1024, 128, 2
+    assert 224.0**2 * D / math.sqrt(D) * 8.0 / math.log(2.0) > 2.0**22
+    gen = torch.Generator().manual_seed(31)
+    signs = torch.randint(0, 2, (1, H, S, D), generator=gen).float() * 2 - 1
+    Q = (224.0 * signs).to(torch.bfloat16).cuda()
+    K = Q.clone()
+    V = torch.randn(1, H, S, D, generator=gen).to(torch.bfloat16).cuda()
+    plan = m.vc_attn_prepare(Q, K, V, 8, 2)
+    O = m.vc_attn_forward(plan)
+    assert m.vc_plan_status(plan) == (0, 0)
+    allp = gpu_plan_all(m, plan)
+    rows = np.arange(S)
+    for h in range(H):
+        g = head_of(allp, 0, h)
+        rel, _ = errors(f64(O[0, h]), oracle_forward_from_plan(g, S, rows))
+        assert rel <= FWD_ONLY_REL, f"head {h}: rel-L2 {rel:.3e}"
     plan.destroy()
