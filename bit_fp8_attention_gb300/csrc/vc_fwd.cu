@@ -226,7 +226,8 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
   const int qt = blockIdx.x, bh = blockIdx.y;
   const int nkb = args.nkb;
   const int npairs = (nkb + 1) / 2;
-  const int start = (args.flags & VC_MIDWINDOW) ? min(nkb - 1, qt + 2) : -1;
+  // Mid-window order shared by the query tiles 2m and 2m+1: start at key tile 2m+2.
+  const int start = (args.flags & VC_MIDWINDOW) ? min(nkb - 1, (qt & ~1) + 2) : -1;
   const bool use_mean = args.use_mean != 0;
 
   if (tid == 0) {

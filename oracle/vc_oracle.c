@@ -24,7 +24,9 @@
  *   R6  The ExpCast pre-round value is computed as one fp32 fused multiply-add
  *       y = fmaf(S32, a_j, 119.65f - M), then rounded to the nearest integer, ties to even, and
  *       clipped to [0, 120]. Codes 1..7 decode as E4M3 subnormals.
- *   R7  Key visit order for query tile qt: start = min(nkb-1, qt+2), sweep down to 0, then the tail.
+ *   R7  Key visit order for query tile qt: start = min(nkb-1, 2*floor(qt/2) + 2), sweep down to 0, then
+ *       the tail. The two query tiles 2m and 2m+1 share one order (2 and 1 blocks past their
+ *       diagonals), so that one pass over the keys can serve both.
  */
 #include <math.h>
 #include <stdint.h>
@@ -300,14 +302,16 @@ void orc_gather_rows(const uint16_t* x, const int32_t* perm, int64_t S, int D, u
 /* ---------------------------------------------------------------------------------------------
  * Key visit order.  [OVC] "Scheduling around ExpCast", mid-window key traversal: start a few
  * blocks past the query's diagonal block, sweep down to block 0, then visit the tail; every block
- * once.  Reading R7: "a few" = 2.  midwindow = 0 gives the linear order 0..nkb-1.
+ * once.  Reading R7: the pair of query tiles (2m, 2m+1) starts at block 2m+2, i.e. "a few" = 2 for
+ * the even tile and 1 for the odd one.  midwindow = 0 gives the linear order 0..nkb-1.
  * ------------------------------------------------------------------------------------------- */
 void orc_visit_order(int nkb, int qt, int midwindow, int32_t* order) {
   if (!midwindow) {
     for (int i = 0; i < nkb; ++i) order[i] = i;
     return;
   }
-  int start = qt + 2 < nkb - 1 ? qt + 2 : nkb - 1;
+  const int pair_start = (qt / 2) * 2 + 2;
+  int start = pair_start < nkb - 1 ? pair_start : nkb - 1;
   int n = 0;
   for (int j = start; j >= 0; --j) order[n++] = j;
   for (int j = start + 1; j < nkb; ++j) order[n++] = j;

@@ -81,7 +81,7 @@ def closed_form(prep, r, expcast=True, midwindow=True, with_mean=True):
     qt = r // 128
     order = list(range(nkb))
     if midwindow:
-        st = min(nkb - 1, qt + 2)
+        st = min(nkb - 1, 2 * (qt // 2) + 2)  # the pair of query tiles (2m, 2m+1) starts at 2m+2
         order = list(range(st, -1, -1)) + list(range(st + 1, nkb))
     C = np.float32(8.0 * LOG2E / math.sqrt(D))
     aq = np.float32(C * prep["sq"][qt])
@@ -227,3 +227,18 @@ def test_mean_restoration_on_quantised_path():
     prep_nomean = dict(prep, vsmooth=False)
     bad, _, _ = oracle.forward_head(prep_nomean, rows)
     assert np.abs(bad - out).max() > 0.1
+
+
+@pytest.mark.parametrize("nkb", [1, 2, 3, 7, 64])
+def test_visit_order_reading(nkb):
+    """Mid-window key traversal ("Open-VC Attention", "Scheduling around ExpCast"): every key tile once,
+    starting a few tiles past the query tile's diagonal, down to tile 0, then the tail in order. Reading:
+    the pair of query tiles (2m, 2m+1) starts at min(nkb-1, 2m+2), so both tiles of a pair share one order."""
+    for qt in range(nkb):
+        o = oracle.visit_order(nkb, qt)
+        start = min(nkb - 1, 2 * (qt // 2) + 2)
+        assert sorted(o.tolist()) == list(range(nkb))
+        assert o[0] == start and start >= min(nkb - 1, qt + 1)
+        assert o.tolist() == list(range(start, -1, -1)) + list(range(start + 1, nkb))
+        assert np.array_equal(o, oracle.visit_order(nkb, qt ^ 1)) or (qt ^ 1) >= nkb
+        assert np.array_equal(oracle.visit_order(nkb, qt, midwindow=False), np.arange(nkb))
