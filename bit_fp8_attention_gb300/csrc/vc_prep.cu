@@ -115,10 +115,14 @@ __global__ void iota_kernel(int32_t* __restrict__ perm, int S, int64_t total) {
 }
 
 // ---------------------------------------------------------------------------------------------
-// Block means of V' = V[pi] and the per-head residual maximum.  One CTA per (block, bh).
-// mu_j = (sum of the valid rows, exact in fp64) / n_j, rounded once to bf16; R = V' - mu_b in
+// Block means of V' = V[pi] and the per-head residual maximum.  One CTA per (block, bh); the block's
+// rows are gathered into shared memory once.
+// mu_j = (sum of the valid rows) / n_j, rounded once to bf16. The sum is exact: every bf16 value is an
+// 8-bit significand M times 2^(E-134); relative to the column's largest exponent E_max it becomes the
+// integer M * 2^(E - E_max + 45) (|sum| < 2^60 in int64), exact whenever the column spans at most 45
+// binades. Whenever an fp64 running sum would be exact too (a span of at most 38 binades), the double
+// (sum * 2^(E_max - 179)) / n_j is then the same double, and so is the bf16 mean. R = V' - mu_b in
 // fp32; amax_h = max |R| over the head (atomicMax on the bit pattern of a non-negative float).
-// ---------------------------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(256) vmeans_kernel(const uint16_t* __restrict__ v, const int32_t* __restrict__ perm,
                                                      int S, int demean, uint16_t* __restrict__ mub,
@@ -131,21 +135,42 @@ __global__ void __launch_bounds__(256) vmeans_kernel(const uint16_t* __restrict_
   const int t0 = j * 128, n = min(128, S - t0);
   const uint16_t* vh = v + (int64_t)bh * S * D;
   const int32_t* ph = perm ? perm + (int64_t)bh * S : nullptr;
-  __shared__ double sums[SPLIT][D];
+  __shared__ __align__(16) uint16_t blk[128][D];
+  __shared__ int emax_part[SPLIT][D];
+  __shared__ long long sums[SPLIT][D];
   __shared__ float mus[D];
   __shared__ float red[8];
-  double s = 0.0;
-  for (int r = part; r < n; r += SPLIT) {
-    int src = ph ? ph[t0 + r] : t0 + r;
-    s += (double)bf16_bits_to_f32(vh[(int64_t)src * D + d]);
+  constexpr int CPR = D / 8;  // 16-byte chunks per row
+  for (int c = threadIdx.x; c < n * CPR; c += 256) {
+    const int r = c / CPR, cc = c % CPR;
+    const int src = ph ? ph[t0 + r] : t0 + r;
+    *reinterpret_cast<uint4*>(&blk[r][cc * 8]) = __ldg(reinterpret_cast<const uint4*>(vh + (int64_t)src * D) + cc);
   }
-  sums[part][d] = s;
+  __syncthreads();
+  // exponent field with subnormals and zero read as 1, as in M * 2^(E - 134)
+  int em = 1;
+  for (int r = part; r < n; r += SPLIT) em = max(em, max((blk[r][d] >> 7) & 0xFF, 1));
+  emax_part[part][d] = em;
+  __syncthreads();
+#pragma unroll
+  for (int q = 0; q < SPLIT; ++q) em = max(em, emax_part[q][d]);
+  long long acc = 0;
+  for (int r = part; r < n; r += SPLIT) {
+    const uint32_t b = blk[r][d];
+    const int e = (b >> 7) & 0xFF;
+    const long long m = (long long)((b & 0x7Fu) | (e ? 0x80u : 0u));
+    const int sh = max(e, 1) - em + 45;  // in [.., 45]; below 0 only past a 45-binade span
+    const long long x = sh >= 0 ? (m << sh) : (m >> min(-sh, 63));
+    acc += (b & 0x8000u) ? -x : x;
+  }
+  sums[part][d] = acc;
   __syncthreads();
   if (part == 0) {
-    double tot = 0.0;
+    long long tot = 0;
 #pragma unroll
     for (int q = 0; q < SPLIT; ++q) tot += sums[q][d];
-    uint16_t b = demean ? f64_to_bf16_rne(tot / (double)n) : (uint16_t)0;
+    const double total = ldexp((double)tot, em - 179);  // 2^(E - 134) * 2^-45
+    uint16_t b = demean ? f64_to_bf16_rne(total / (double)n) : (uint16_t)0;
     mub[((int64_t)bh * nkb + j) * D + d] = b;
     if (mubT) mubT[((int64_t)bh * D + d) * nkb16 + j] = b;  // [BH, D, nkb16]: the forward's flush operand
     mus[d] = bf16_bits_to_f32(b);
@@ -153,8 +178,7 @@ __global__ void __launch_bounds__(256) vmeans_kernel(const uint16_t* __restrict_
   __syncthreads();
   float amax = 0.f;
   for (int r = part; r < n; r += SPLIT) {
-    int src = ph ? ph[t0 + r] : t0 + r;
-    float res = __fsub_rn(bf16_bits_to_f32(vh[(int64_t)src * D + d]), mus[d]);
+    float res = __fsub_rn(bf16_bits_to_f32(blk[r][d]), mus[d]);
     amax = fmaxf(amax, fabsf(res));
   }
   for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -168,8 +192,9 @@ __global__ void __launch_bounds__(256) vmeans_kernel(const uint16_t* __restrict_
 }
 
 // Residual codes, transposed: Vt[bh][d][t] = E4M3(R[t][d] * 448/amax_h), t < S_pad (pad = 0).
-// One CTA per (block, bh); the 128 x D code tile is transposed through shared memory so that
-// each d-row of 128 codes is written with one coalesced 128-byte store.
+// One CTA per (block, bh): the block's rows are gathered into shared memory with 16-byte loads, then
+// each thread codes 32 rows of one channel (reads along the channels are conflict-free) and writes
+// them as one 32-byte sector of the transposed output.
 template <int D>
 __global__ void __launch_bounds__(256) vpack_kernel(const uint16_t* __restrict__ v, const int32_t* __restrict__ perm,
                                                     int S, int S_pad, const uint16_t* __restrict__ mub,
@@ -177,46 +202,43 @@ __global__ void __launch_bounds__(256) vpack_kernel(const uint16_t* __restrict__
                                                     uint8_t* __restrict__ vt, float* __restrict__ sv) {
   const int j = blockIdx.x, bh = blockIdx.y;
   const int nkb = S_pad / 128;
+  const int t0 = j * 128, n = min(128, S - t0);
   const uint16_t* vh = v + (int64_t)bh * S * D;
   const int32_t* ph = perm ? perm + (int64_t)bh * S : nullptr;
-  __shared__ uint8_t tile[D][128 + 16];
+  __shared__ __align__(16) uint16_t blk[128][D];
+  __shared__ float mus[D];
   const float amax = __uint_as_float(amax_bits[bh]);
   const bool zero = !(amax > 0.f);
   const float inv = zero ? 1.f : __fdiv_rn(448.f, amax);
   if (j == 0 && threadIdx.x == 0) sv[bh] = zero ? 1.f : __fdiv_rn(amax, 448.f);
-  const uint16_t* mu = mub + ((int64_t)bh * nkb + j) * D;
-  // each thread converts 8 consecutive channels of one row (one 16-byte load)
-  constexpr int CPR = D / 8;
-  for (int c = threadIdx.x; c < 128 * CPR; c += 256) {
-    int r = c / CPR, cc = c % CPR;
-    int t = j * 128 + r;
-    uint32_t codes2[4] = {0, 0, 0, 0};
-    if (t < S) {
-      int src = ph ? ph[t] : t;
-      uint4 raw = *reinterpret_cast<const uint4*>(vh + (int64_t)src * D + cc * 8);
-      uint4 mraw = *reinterpret_cast<const uint4*>(mu + cc * 8);
-      const uint32_t* w = reinterpret_cast<const uint32_t*>(&raw);
-      const uint32_t* mw = reinterpret_cast<const uint32_t*>(&mraw);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float r0 = __fsub_rn(bf16_bits_to_f32(w[q] & 0xFFFFu), bf16_bits_to_f32(mw[q] & 0xFFFFu));
-        float r1 = __fsub_rn(bf16_bits_to_f32(w[q] >> 16), bf16_bits_to_f32(mw[q] >> 16));
-        codes2[q] = cvt_e4m3x2(__fmul_rn(r0, inv), __fmul_rn(r1, inv));
-      }
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      tile[cc * 8 + 2 * q][r] = (uint8_t)(codes2[q] & 0xFF);
-      tile[cc * 8 + 2 * q + 1][r] = (uint8_t)(codes2[q] >> 8);
-    }
+  constexpr int CPR = D / 8;  // 16-byte chunks per row
+  for (int c = threadIdx.x; c < n * CPR; c += 256) {
+    const int r = c / CPR, cc = c % CPR;
+    const int src = ph ? ph[t0 + r] : t0 + r;
+    *reinterpret_cast<uint4*>(&blk[r][cc * 8]) = __ldg(reinterpret_cast<const uint4*>(vh + (int64_t)src * D) + cc);
   }
+  for (int d = threadIdx.x; d < D; d += 256) mus[d] = bf16_bits_to_f32(mub[((int64_t)bh * nkb + j) * D + d]);
   __syncthreads();
-  // write D rows of 128 bytes: 8 threads per row, 16 bytes each
-  uint8_t* out = vt + (int64_t)bh * D * S_pad + (int64_t)j * 128;
-  for (int c = threadIdx.x; c < D * 8; c += 256) {
-    int d = c / 8, seg = c % 8;
-    uint4 val = *reinterpret_cast<const uint4*>(&tile[d][seg * 16]);
-    *reinterpret_cast<uint4*>(out + (int64_t)d * S_pad + seg * 16) = val;
+  uint8_t* out = vt + (int64_t)bh * D * S_pad + (int64_t)t0;
+  for (int task = threadIdx.x; task < D * 4; task += 256) {
+    const int d = task % D, seg = task / D;  // rows [32 seg, 32 seg + 32) of channel d
+    const float mu = mus[d];
+    uint32_t w[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int r = seg * 32 + 4 * q + 2 * h;
+        const float r0 = r < n ? __fmul_rn(__fsub_rn(bf16_bits_to_f32(blk[r][d]), mu), inv) : 0.f;
+        const float r1 = r + 1 < n ? __fmul_rn(__fsub_rn(bf16_bits_to_f32(blk[r + 1][d]), mu), inv) : 0.f;
+        word |= cvt_e4m3x2(r0, r1) << (16 * h);
+      }
+      w[q] = word;
+    }
+    uint4* dst = reinterpret_cast<uint4*>(out + (int64_t)d * S_pad + seg * 32);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
   }
 }
 
