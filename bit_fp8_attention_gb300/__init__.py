@@ -29,6 +29,7 @@ VC_ERR_NO_DEVICE = -7
 VC_EXPCAST = 1
 VC_VSMOOTH = 2
 VC_MIDWINDOW = 4
+VC_KCENTER = 8
 VC_DEBUG_TIMEOUT = 1 << 16
 VC_FLAGS_DEFAULT = VC_EXPCAST | VC_VSMOOTH | VC_MIDWINDOW
 
@@ -42,6 +43,7 @@ VC_PLAN_VCODES = 7
 VC_PLAN_VSCALES = 8
 VC_PLAN_MEANS = 9
 VC_PLAN_CENTROIDS = 10
+VC_PLAN_KCENTER = 11
 VC_NOALLOC_MAX_HEADS = 4096
 
 EXPORTS = ("vc_attn_prepare", "vc_attn_prepare_ex", "vc_attn_forward", "vc_plan_size", "vc_plan_get",
@@ -187,6 +189,7 @@ _PLAN_DTYPES = {
     VC_PLAN_VSCALES: (torch.float32, lambda p: (p.B, p.H)),
     VC_PLAN_MEANS: (torch.bfloat16, lambda p: (p.B, p.H, p.nkb, p.D)),
     VC_PLAN_CENTROIDS: (torch.float32, lambda p: (p.B, p.H, p.k, p.D)),
+    VC_PLAN_KCENTER: (torch.bfloat16, lambda p: (p.B, p.H, p.D)),
 }
 
 

@@ -77,6 +77,9 @@ int plan_create(int B, int H, int S, int D, int k, vc_plan** out) {
       BH * 2 * b.kpad * D * 2,        // cent16
       BH * b.kpad * 4,                // cnormp
       BH * b.nchunk * k * 4,          // chist
+      BH * D * 4,                     // kexp
+      BH * D * 8,                     // ksum
+      BH * D * 2,                     // kmu
       BH * 4,                         // vamax
       16,                             // status
   };
@@ -93,6 +96,7 @@ int plan_create(int B, int H, int S, int D, int k, vc_plan** out) {
                     (void**)&b.vcodes, (void**)&b.vscales, (void**)&b.means,   (void**)&b.meansT, (void**)&b.labels,
                     (void**)&b.perm,   (void**)&b.cent,    (void**)&b.cnorm,   (void**)&b.counts,
                     (void**)&b.offsets, (void**)&b.cent16, (void**)&b.cnormp,  (void**)&b.chist,
+                    (void**)&b.kexp,   (void**)&b.ksum,    (void**)&b.kmu,
                     (void**)&b.vamax,  (void**)&b.status};
   for (size_t i = 0; i < sizeof(sizes) / sizeof(sizes[0]); ++i) {
     *slots[i] = p;
@@ -140,8 +144,9 @@ int vc_attn_prepare_ex(const void* Q, const void* K, const void* V, int B, int H
   }
   vc_plan* pl = *plan;
   pl->b.has_means = vsmooth;
+  pl->b.has_kcenter = (flags & VC_KCENTER) != 0;
   return vc::prepare_launch(pl->b, (const uint16_t*)Q, (const uint16_t*)K, (const uint16_t*)V,
-                            vsmooth ? perm : nullptr, vsmooth, iters, stream);
+                            vsmooth ? perm : nullptr, vsmooth, pl->b.has_kcenter, iters, stream);
 }
 
 int vc_attn_prepare(const void* Q, const void* K, const void* V, int B, int H, int S, int D, int k_clusters,
@@ -171,6 +176,7 @@ size_t vc_plan_size(const vc_plan* plan, int what) {
     case VC_PLAN_VSCALES: return BH * 4;
     case VC_PLAN_MEANS: return BH * b.nkb * b.D * 2;
     case VC_PLAN_CENTROIDS: return BH * b.k * b.D * 4;
+    case VC_PLAN_KCENTER: return BH * b.D * 2;
     default: return 0;
   }
 }
@@ -191,6 +197,7 @@ int vc_plan_get(const vc_plan* plan, int what, void* dst, size_t bytes, cudaStre
     case VC_PLAN_VSCALES: src = b.vscales; break;
     case VC_PLAN_MEANS: src = b.means; break;
     case VC_PLAN_CENTROIDS: src = b.cent; break;
+    case VC_PLAN_KCENTER: src = b.kmu; break;
   }
   return cudaMemcpyAsync(dst, src, n, cudaMemcpyDefault, stream) == cudaSuccess ? VC_OK : VC_ERR_CUDA;
 }

@@ -31,13 +31,17 @@ struct PlanBuffers {
   int32_t* chist;       // [BH, nchunk, k] per-chunk label counts, then chunk start positions
   int32_t* counts;      // [BH, k]
   int32_t* offsets;     // [BH, k]
+  int* kexp;            // [BH, D] largest bf16 exponent of each K channel (centering statistic)
+  unsigned long long* ksum;  // [BH, D] exact fixed-point channel sums of K
+  uint16_t* kmu;        // [BH, D] bf16 channel centre of K
+  bool has_kcenter;     // prepared with K centering
   unsigned int* vamax;  // [BH] residual |max| as float bits
   int* status;          // [1]
   bool has_means;       // prepared with V-Smooth
 };
 
 int prepare_launch(const PlanBuffers& p, const uint16_t* Q, const uint16_t* K, const uint16_t* V,
-                   const int32_t* perm_in, bool vsmooth, int iters, cudaStream_t st);
+                   const int32_t* perm_in, bool vsmooth, bool kcenter, int iters, cudaStream_t st);
 
 int kmeans_launch(const PlanBuffers& p, const uint16_t* V, int iters, cudaStream_t st);
 int kmeans_chunks(int S);

@@ -49,9 +49,23 @@ static __device__ uint16_t f64_to_bf16_rne(double x) {
 // when it is given (the K' = K[pi] gather), otherwise in order.  amax over the whole 128 x D
 // block, scale = amax/448, code = E4M3_rne_satfinite(x * (448/amax)); pad rows get code 0.
 // ---------------------------------------------------------------------------------------------
+// One element of a 16-byte chunk of 8 bf16, as fp32, minus the matching centre element if any.
+__device__ __forceinline__ float chunk_elem(const uint4& w, const uint4& c, bool centred, int i) {
+  const uint32_t* wv = reinterpret_cast<const uint32_t*>(&w);
+  const uint32_t* cv = reinterpret_cast<const uint32_t*>(&c);
+  const int sh = (i & 1) * 16;
+  float f = bf16_bits_to_f32((wv[i >> 1] >> sh) & 0xFFFFu);
+  if (centred) f = __fsub_rn(f, bf16_bits_to_f32((cv[i >> 1] >> sh) & 0xFFFFu));
+  return f;
+}
+
+// Per-128-token block E4M3 quantisation of Q (token order) or K (gathered through pi, optionally minus
+// the head's channel centre): one CTA per (block, bh), amax over the valid rows, scale = amax/448,
+// code = E4M3_RNE_sat(x * (448/amax)); pad rows are code 0.
 template <int D>
 __global__ void __launch_bounds__(256) quant_blocks_kernel(const uint16_t* __restrict__ x,
-                                                           const int32_t* __restrict__ perm, int S, int S_pad,
+                                                           const int32_t* __restrict__ perm,
+                                                           const uint16_t* __restrict__ center, int S, int S_pad,
                                                            uint8_t* __restrict__ codes, float* __restrict__ scales) {
   constexpr int CPR = D / 8;                 // 16-byte chunks per row
   constexpr int NCH = 128 * CPR / 256;       // chunks per thread
@@ -59,24 +73,20 @@ __global__ void __launch_bounds__(256) quant_blocks_kernel(const uint16_t* __res
   const int nkb = S_pad / 128;
   const uint16_t* xh = x + (int64_t)bh * S * D;
   const int32_t* ph = perm ? perm + (int64_t)bh * S : nullptr;
-  uint4 v[NCH];
+  const bool centred = center != nullptr;
+  uint4 v[NCH], cen[NCH];
   float amax = 0.f;
 #pragma unroll
   for (int m = 0; m < NCH; ++m) {
     int c = threadIdx.x + 256 * m;
     int r = c / CPR, cc = c % CPR;
     int t = j * 128 + r;
+    cen[m] = centred ? __ldg(reinterpret_cast<const uint4*>(center + (int64_t)bh * D) + cc) : make_uint4(0, 0, 0, 0);
     if (t < S) {
       int src = ph ? ph[t] : t;
       v[m] = *reinterpret_cast<const uint4*>(xh + (int64_t)src * D + cc * 8);
-    } else {
-      v[m] = make_uint4(0, 0, 0, 0);
-    }
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(&v[m]);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w[q] & 0xFFFFu)));
-      amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w[q] >> 16)));
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(chunk_elem(v[m], cen[m], centred, i)));
     }
   }
   __shared__ float red[8];
@@ -95,18 +105,81 @@ __global__ void __launch_bounds__(256) quant_blocks_kernel(const uint16_t* __res
   for (int m = 0; m < NCH; ++m) {
     int c = threadIdx.x + 256 * m;
     int r = c / CPR, cc = c % CPR;
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(&v[m]);
     uint32_t lo = 0, hi = 0;
-    if (!zero) {
-      lo = cvt_e4m3x2(__fmul_rn(bf16_bits_to_f32(w[0] & 0xFFFFu), inv), __fmul_rn(bf16_bits_to_f32(w[0] >> 16), inv)) |
-           (cvt_e4m3x2(__fmul_rn(bf16_bits_to_f32(w[1] & 0xFFFFu), inv), __fmul_rn(bf16_bits_to_f32(w[1] >> 16), inv))
-            << 16);
-      hi = cvt_e4m3x2(__fmul_rn(bf16_bits_to_f32(w[2] & 0xFFFFu), inv), __fmul_rn(bf16_bits_to_f32(w[2] >> 16), inv)) |
-           (cvt_e4m3x2(__fmul_rn(bf16_bits_to_f32(w[3] & 0xFFFFu), inv), __fmul_rn(bf16_bits_to_f32(w[3] >> 16), inv))
-            << 16);
+    if (!zero && j * 128 + r < S) {
+      uint32_t w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        w[q] = cvt_e4m3x2(__fmul_rn(chunk_elem(v[m], cen[m], centred, 2 * q), inv),
+                          __fmul_rn(chunk_elem(v[m], cen[m], centred, 2 * q + 1), inv));
+      lo = w[0] | (w[1] << 16);
+      hi = w[2] | (w[3] << 16);
     }
     *reinterpret_cast<uint2*>(ch + (int64_t)r * D + cc * 8) = make_uint2(lo, hi);
   }
+}
+
+// ---------------------------------------------------------------------------------------------
+// K channel centre ("VC-Attention", Sec. 3.4 "Fused preprocessing" and App. B: the K pass gathers
+// centering statistics and subtracts the mean): mu[bh][d] = bf16_RNE(sum_t K[t][d] / S). The sum is
+// taken exactly in int64: each bf16 is M * 2^(E - 134) with an 8-bit significand M; relative to the
+// column's largest exponent E_max it is M * 2^(E - E_max + 28) (|sum| < 2^56 for S <= 2^20), so only
+// values more than 28 binades below the column maximum lose low bits.
+// ---------------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) kstat_exp_kernel(const uint16_t* __restrict__ x, int S, int* __restrict__ kexp) {
+  constexpr int SPLIT = 256 / D;
+  const int j = blockIdx.x, bh = blockIdx.y;
+  const int d = threadIdx.x % D, part = threadIdx.x / D;
+  const int t0 = j * 128, n = min(128, S - t0);
+  const uint16_t* xh = x + ((int64_t)bh * S + t0) * D;
+  __shared__ int ep[SPLIT][D];
+  int em = 1;
+  for (int r = part; r < n; r += SPLIT) em = max(em, max((xh[(int64_t)r * D + d] >> 7) & 0xFF, 1));
+  ep[part][d] = em;
+  __syncthreads();
+  if (part == 0) {
+#pragma unroll
+    for (int q = 1; q < SPLIT; ++q) em = max(em, ep[q][d]);
+    atomicMax(kexp + (int64_t)bh * D + d, em);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) kstat_sum_kernel(const uint16_t* __restrict__ x, int S,
+                                                        const int* __restrict__ kexp,
+                                                        unsigned long long* __restrict__ ksum) {
+  constexpr int SPLIT = 256 / D;
+  const int j = blockIdx.x, bh = blockIdx.y;
+  const int d = threadIdx.x % D, part = threadIdx.x / D;
+  const int t0 = j * 128, n = min(128, S - t0);
+  const uint16_t* xh = x + ((int64_t)bh * S + t0) * D;
+  const int em = kexp[(int64_t)bh * D + d];
+  __shared__ long long sp[SPLIT][D];
+  long long acc = 0;
+  for (int r = part; r < n; r += SPLIT) {
+    const uint32_t b = xh[(int64_t)r * D + d];
+    const int e = (b >> 7) & 0xFF;
+    const long long m = (long long)((b & 0x7Fu) | (e ? 0x80u : 0u));
+    const int sh = max(e, 1) - em + 28;
+    const long long xv = sh >= 0 ? (m << sh) : (m >> min(-sh, 63));
+    acc += (b & 0x8000u) ? -xv : xv;
+  }
+  sp[part][d] = acc;
+  __syncthreads();
+  if (part == 0) {
+#pragma unroll
+    for (int q = 1; q < SPLIT; ++q) acc += sp[q][d];
+    atomicAdd(ksum + (int64_t)bh * D + d, (unsigned long long)acc);  // two's complement: order-free
+  }
+}
+
+__global__ void kstat_mean_kernel(const int* __restrict__ kexp, const unsigned long long* __restrict__ ksum, int S,
+                                  int n, uint16_t* __restrict__ kmu) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const double total = ldexp((double)(long long)ksum[i], kexp[i] - 162);  // 2^(E - 134) * 2^-28
+  kmu[i] = f64_to_bf16_rne(total / (double)S);
 }
 
 __global__ void iota_kernel(int32_t* __restrict__ perm, int S, int64_t total) {
@@ -248,12 +321,12 @@ __global__ void __launch_bounds__(256) vpack_kernel(const uint16_t* __restrict__
 static int check_launch() { return cudaPeekAtLastError() == cudaSuccess ? 0 : VC_ERR_CUDA; }
 
 int prepare_launch(const PlanBuffers& p, const uint16_t* Q, const uint16_t* K, const uint16_t* V,
-                   const int32_t* perm_in, bool vsmooth, int iters, cudaStream_t st) {
+                   const int32_t* perm_in, bool vsmooth, bool kcenter, int iters, cudaStream_t st) {
   const int BH = p.B * p.H, S = p.S, D = p.D, nkb = p.nkb, S_pad = p.S_pad;
   dim3 gblk(nkb, BH);
   // Q: per-block quantisation in token order
-  if (D == 128) quant_blocks_kernel<128><<<gblk, 256, 0, st>>>(Q, nullptr, S, S_pad, p.qcodes, p.qscales);
-  else quant_blocks_kernel<64><<<gblk, 256, 0, st>>>(Q, nullptr, S, S_pad, p.qcodes, p.qscales);
+  if (D == 128) quant_blocks_kernel<128><<<gblk, 256, 0, st>>>(Q, nullptr, nullptr, S, S_pad, p.qcodes, p.qscales);
+  else quant_blocks_kernel<64><<<gblk, 256, 0, st>>>(Q, nullptr, nullptr, S, S_pad, p.qcodes, p.qscales);
   if (check_launch()) return VC_ERR_CUDA;
   const int32_t* perm = nullptr;
   if (vsmooth) {
@@ -272,8 +345,23 @@ int prepare_launch(const PlanBuffers& p, const uint16_t* Q, const uint16_t* K, c
   }
   if (check_launch()) return VC_ERR_CUDA;
   // K' = K[pi], per-block quantisation
-  if (D == 128) quant_blocks_kernel<128><<<gblk, 256, 0, st>>>(K, perm, S, S_pad, p.kcodes, p.kscales);
-  else quant_blocks_kernel<64><<<gblk, 256, 0, st>>>(K, perm, S, S_pad, p.kcodes, p.kscales);
+  const uint16_t* kcen = nullptr;
+  if (kcenter) {  // the head's channel centre of K, in token order
+    if (cudaMemsetAsync(p.kexp, 0, sizeof(int) * (size_t)BH * D, st) != cudaSuccess ||
+        cudaMemsetAsync(p.ksum, 0, sizeof(unsigned long long) * (size_t)BH * D, st) != cudaSuccess)
+      return VC_ERR_CUDA;
+    if (D == 128) {
+      kstat_exp_kernel<128><<<gblk, 256, 0, st>>>(K, S, p.kexp);
+      kstat_sum_kernel<128><<<gblk, 256, 0, st>>>(K, S, p.kexp, p.ksum);
+    } else {
+      kstat_exp_kernel<64><<<gblk, 256, 0, st>>>(K, S, p.kexp);
+      kstat_sum_kernel<64><<<gblk, 256, 0, st>>>(K, S, p.kexp, p.ksum);
+    }
+    kstat_mean_kernel<<<(BH * D + 255) / 256, 256, 0, st>>>(p.kexp, p.ksum, S, BH * D, p.kmu);
+    kcen = p.kmu;
+  }
+  if (D == 128) quant_blocks_kernel<128><<<gblk, 256, 0, st>>>(K, perm, kcen, S, S_pad, p.kcodes, p.kscales);
+  else quant_blocks_kernel<64><<<gblk, 256, 0, st>>>(K, perm, kcen, S, S_pad, p.kcodes, p.kscales);
   // V' = V[pi]: block means, residual maximum per head, residual codes transposed
   if (cudaMemsetAsync(p.vamax, 0, sizeof(unsigned int) * BH, st) != cudaSuccess) return VC_ERR_CUDA;
   if (D == 128) {

@@ -56,9 +56,14 @@ enum {
   /* V-Smooth (Sec. 3.2): k-means grouping, permutation of K and V, 128-row block means
      restored in the accumulator. Off (prepare): identity permutation and no means. */
   VC_VSMOOTH = 2u,
-  /* Mid-window key order ("Open-VC Attention", mid-window key traversal): query tile qt starts
-     at key tile min(nkb-1, qt+2), sweeps down to tile 0, then visits the tail. Off: 0..nkb-1. */
+  /* Mid-window key order ("Open-VC Attention", mid-window key traversal): the query tiles 2m and
+     2m+1 share one order that starts at key tile min(nkb-1, 2m+2), sweeps down to tile 0, then
+     visits the tail. Off: 0..nkb-1. */
   VC_MIDWINDOW = 4u,
+  /* Prepare only: K channel centering (VC-Attention Sec. 3.4 "Fused preprocessing", App. B). Every
+     key has the head's channel mean mu (bf16 of the exact mean over the S tokens) subtracted in fp32
+     before its block quantisation; the softmax is unchanged, the keys' quantisation range shrinks. */
+  VC_KCENTER = 8u,
   /* Test hook: the forward kernel's first internal wait gives up at once, so the call reports
      VC_ERR_TIMEOUT through vc_plan_status() without hanging. */
   VC_DEBUG_TIMEOUT = 1u << 16
@@ -96,7 +101,8 @@ int vc_attn_prepare(const void* Q, const void* K, const void* V, int B, int H, i
  *   (reusing the permutation across denoising steps, VC-Attention Sec. 3.4 "Amortized grouping
  *   schedule"; it is not checked to be a permutation -- every entry must lie in [0, S)).
  * flags: VC_VSMOOTH set -> group (unless perm is given) and demean; clear -> identity
- *   permutation (perm ignored), no means, R = V.  Other bits are ignored here. */
+ *   permutation (perm ignored), no means, R = V.  VC_KCENTER set -> subtract the keys' channel
+ *   centre before their quantisation.  Other bits are ignored here. */
 int vc_attn_prepare_ex(const void* Q, const void* K, const void* V, int B, int H, int S, int D, int k_clusters,
                        int iters, const int32_t* perm, unsigned flags, cudaStream_t stream, vc_plan** plan);
 
@@ -125,7 +131,8 @@ enum {
   VC_PLAN_VCODES = 7,    /* uint8 [B, H, D, S_pad] E4M3 codes of the residual, transposed     */
   VC_PLAN_VSCALES = 8,   /* fp32  [B, H]           per-head residual scale                    */
   VC_PLAN_MEANS = 9,     /* bf16  [B, H, nkb, D]   block means of V'                          */
-  VC_PLAN_CENTROIDS = 10 /* fp32  [B, H, k, D]     centroids after the last update           */
+  VC_PLAN_CENTROIDS = 10, /* fp32 [B, H, k, D]     centroids after the last update           */
+  VC_PLAN_KCENTER = 11   /* bf16  [B, H, D]        K channel centre (prepared with VC_KCENTER) */
 };
 /* Size in bytes of one plan tensor (0 for an unknown `what` or a NULL plan). */
 size_t vc_plan_size(const vc_plan* plan, int what);

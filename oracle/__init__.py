@@ -70,6 +70,8 @@ def lib():
             "orc_exp_then_cast": (ctypes.c_uint8, [ctypes.c_double]),
             "orc_expcast_of_u": (ctypes.c_int, [ctypes.c_double]),
             "orc_quant_blocks": (None, [u16, ctypes.c_int64, ctypes.c_int, u8, f32]),
+            "orc_quant_blocks_centered": (None, [u16, ctypes.c_int64, ctypes.c_int, u16, u8, f32]),
+            "orc_channel_mean_bf16": (None, [u16, ctypes.c_int64, ctypes.c_int, u16]),
             "orc_kmeans_objective": (ctypes.c_double, [u16, ctypes.c_int64, ctypes.c_int, ctypes.c_int, i32]),
             "orc_kmeans": (None, [u16, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, i32, f64, f64]),
             "orc_stable_argsort": (None, [i32, ctypes.c_int64, ctypes.c_int, i32]),
@@ -185,18 +187,32 @@ def code_scale(D: int) -> float:
 # ----------------------------------------------------------------------------------------------
 # Preparation steps
 # ----------------------------------------------------------------------------------------------
-def quant_blocks(x) -> tuple[np.ndarray, np.ndarray]:
+def quant_blocks(x, center=None) -> tuple[np.ndarray, np.ndarray]:
     """Per-128-token block E4M3 quantisation ([OVC] "Scheduling around ExpCast").
 
-    x: [S, D] bf16. Returns codes [S_pad, D] uint8 and scales [nkb] float32.
+    x: [S, D] bf16. center: None, or [D] bf16 subtracted (fp32) from every row first.
+    Returns codes [S_pad, D] uint8 and scales [nkb] float32.
     """
     x = _u16(x)
     S, D = x.shape
     nkb = nkb_of(S)
     codes = np.empty((nkb * BLOCK, D), dtype=np.uint8)
     scales = np.empty(nkb, dtype=np.float32)
-    lib().orc_quant_blocks(_ptr(x, ctypes.c_uint16), S, D, _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_float))
+    c = None if center is None else np.ascontiguousarray(_u16(center).reshape(D))
+    lib().orc_quant_blocks_centered(_ptr(x, ctypes.c_uint16), S, D,
+                                    None if c is None else _ptr(c, ctypes.c_uint16),
+                                    _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_float))
     return codes, scales
+
+
+def channel_mean_bf16(x) -> np.ndarray:
+    """K channel centering statistic ([VC] §3.4 "Fused preprocessing", App. B): bf16 of the fp64 mean
+    of every channel over the head's tokens. x: [S, D] bf16. Returns [D] bf16 bits (uint16)."""
+    x = _u16(x)
+    S, D = x.shape
+    mu = np.empty(D, dtype=np.uint16)
+    lib().orc_channel_mean_bf16(_ptr(x, ctypes.c_uint16), S, D, _ptr(mu, ctypes.c_uint16))
+    return mu
 
 
 def kmeans(v, k: int, iters: int):
@@ -324,11 +340,13 @@ def attention_demeaned_exact(q, k, v, rows, midwindow: bool = True) -> np.ndarra
 # ----------------------------------------------------------------------------------------------
 # Whole-path conveniences for one batch-head
 # ----------------------------------------------------------------------------------------------
-def prepare_head(q, k, v, k_clusters: int, iters: int, vsmooth: bool = True, perm=None) -> dict:
+def prepare_head(q, k, v, k_clusters: int, iters: int, vsmooth: bool = True, perm=None,
+                 kcenter: bool = False) -> dict:
     """Everything the prepare step produces for one batch-head, computed on the CPU.
 
     vsmooth=False: identity permutation, no means (R = V). perm given: use it instead of k-means
     (the parity tests feed the GPU's permutation here, as the acceptance rule says).
+    kcenter: subtract the keys' channel mean before their quantisation (see channel_mean_bf16).
     """
     q, k, v = _u16(q), _u16(k), _u16(v)
     S, D = q.shape
@@ -344,7 +362,9 @@ def prepare_head(q, k, v, k_clusters: int, iters: int, vsmooth: bool = True, per
     out["perm"] = perm
     out["qc"], out["sq"] = quant_blocks(q)
     kp = gather_rows(k, perm)
-    out["kc"], out["sk"] = quant_blocks(kp)
+    kmu = channel_mean_bf16(k) if kcenter else None
+    out["kmu"] = kmu
+    out["kc"], out["sk"] = quant_blocks(kp, center=kmu)
     dm = demean(v, perm, subtract_mean=vsmooth)
     out.update(rc=dm["rc"], sv=dm["sv"], amax=dm["amax"], mub=dm["mub"], mu=dm["mu"], resid=dm["resid"])
     out["vsmooth"] = vsmooth

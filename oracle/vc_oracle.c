@@ -146,7 +146,10 @@ int orc_expcast_of_u(double u) {
  * 448/amax computed once in fp32, code = E4M3(x * inv).  An all-zero block gets s = 1.
  * x: [S, D] bf16 bits, codes: [S_pad, D] (pad rows zero), scales: [nkb].
  * ------------------------------------------------------------------------------------------- */
-void orc_quant_blocks(const uint16_t* x, int64_t S, int D, uint8_t* codes, float* scales) {
+/* center: NULL, or one bf16 value per channel subtracted (in fp32) from every row before the
+ * block maximum and the codes are taken (the K channel centering below). */
+void orc_quant_blocks_centered(const uint16_t* x, int64_t S, int D, const uint16_t* center, uint8_t* codes,
+                               float* scales) {
   int64_t nkb = (S + ORC_BLOCK - 1) / ORC_BLOCK;
   memset(codes, 0, (size_t)(nkb * ORC_BLOCK * D));
   for (int64_t j = 0; j < nkb; ++j) {
@@ -154,7 +157,9 @@ void orc_quant_blocks(const uint16_t* x, int64_t S, int D, uint8_t* codes, float
     float amax = 0.0f;
     for (int64_t t = t0; t < t1; ++t)
       for (int d = 0; d < D; ++d) {
-        float v = fabsf(bf16_to_f32(x[t * D + d]));
+        float v = bf16_to_f32(x[t * D + d]);
+        if (center) v = v - bf16_to_f32(center[d]);
+        v = fabsf(v);
         if (v > amax) amax = v;
       }
     if (amax == 0.0f) { scales[j] = 1.0f; continue; }
@@ -162,9 +167,30 @@ void orc_quant_blocks(const uint16_t* x, int64_t S, int D, uint8_t* codes, float
     scales[j] = amax / 448.0f;
     for (int64_t t = t0; t < t1; ++t)
       for (int d = 0; d < D; ++d) {
-        float v = bf16_to_f32(x[t * D + d]) * inv;
-        codes[t * D + d] = orc_e4m3_encode(v);
+        float v = bf16_to_f32(x[t * D + d]);
+        if (center) v = v - bf16_to_f32(center[d]);
+        codes[t * D + d] = orc_e4m3_encode(v * inv);
       }
+  }
+}
+
+void orc_quant_blocks(const uint16_t* x, int64_t S, int D, uint8_t* codes, float* scales) {
+  orc_quant_blocks_centered(x, S, D, NULL, codes, scales);
+}
+
+/* ---------------------------------------------------------------------------------------------
+ * K channel centering.  [VC] §3.4 "Fused preprocessing" and App. B: the K quantisation pass fuses
+ * "the centering statistics" and "mean subtraction".  Subtracting one vector from every key adds a
+ * per-query constant to the scores, which the softmax ignores, while the keys' quantisation range
+ * shrinks.  Reading: the statistic is the channel mean over the S tokens of the head, taken in fp64
+ * and rounded once to bf16 (mu[d]); the keys are quantised as K - mu in fp32.
+ * x: [S, D] bf16 bits, token order.  mu: [D] bf16 bits.
+ * ------------------------------------------------------------------------------------------- */
+void orc_channel_mean_bf16(const uint16_t* x, int64_t S, int D, uint16_t* mu) {
+  for (int d = 0; d < D; ++d) {
+    double acc = 0.0;
+    for (int64_t t = 0; t < S; ++t) acc += (double)bf16_to_f32(x[t * D + d]);
+    mu[d] = orc_f64_to_bf16(acc / (double)S);
   }
 }
 

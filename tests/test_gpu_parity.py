@@ -222,3 +222,33 @@ def test_huge_scores_take_the_clamped_code_path(m):
         rel, _ = errors(f64(O[0, h]), oracle_forward_from_plan(g, S, rows))
         assert rel <= FWD_ONLY_REL, f"head {h}: rel-L2 {rel:.3e}"
     plan.destroy()
+
+
+@pytest.mark.parametrize("S,D", [(3000, 64), (2049, 128)])
+def test_k_centering(m, S, D):
+    """VC_KCENTER ("VC-Attention", Sec. 3.4 "Fused preprocessing", App. B): keys with large per-channel
+    offsets. The GPU's channel centre and every prepare output are bit-exact against the oracle fed the
+    GPU's permutation, and the forward meets the acceptance bound."""
+    cfg = synth.custom(S, D=D, H=2, k=max(1, S // 128), iters=2)
+    Q, K, V = synth.make_inputs(cfg, seed=11, device="cuda")
+    gen = torch.Generator().manual_seed(12)
+    offset = (torch.randn(D, generator=gen) * 8.0).cuda()
+    K = (K.float() + offset).to(torch.bfloat16).contiguous()
+    plan = m.vc_attn_prepare_ex(Q, K, V, cfg["k"], cfg["iters"], flags=m.VC_VSMOOTH | m.VC_KCENTER)
+    O = m.vc_attn_forward(plan)
+    assert m.vc_plan_status(plan) == (0, 0)
+    allp = gpu_plan_all(m, plan)
+    kmu = u16(m.vc_plan_get(plan, m.VC_PLAN_KCENTER))
+    rows = np.arange(S)
+    for h in range(2):
+        g = head_of(allp, 0, h)
+        o = oracle.prepare_head(u16(Q[0, h]), u16(K[0, h]), u16(V[0, h]), cfg["k"], cfg["iters"], perm=g["perm"],
+                                kcenter=True)
+        assert np.array_equal(kmu[0, h], o["kmu"]), f"head {h}: channel centre"
+        compare_prep(g, o, S)
+        ref, _, _ = oracle.forward_head(o, rows)
+        got = f64(O[0, h])
+        assert_within(got, ref, float(np.abs(f64(V[0, h])).max()), f"head {h}")
+        rel_f, _ = errors(got, oracle_forward_from_plan(g, S, rows))
+        assert rel_f <= FWD_ONLY_REL, f"head {h}: forward-only rel-L2 {rel_f:.3e}"
+    plan.destroy()
