@@ -301,6 +301,21 @@ def main():
     t_prep_full = time_it(lambda: vc.vc_attn_prepare(Q, K, V, cfg["k"], cfg["iters"], plan=plan))
     t_prep_quant = time_it(lambda: vc.vc_attn_prepare_ex(Q, K, V, cfg["k"], cfg["iters"], perm=perm, plan=plan))
     t_group = max(t_prep_full - t_prep_quant, 0.0)
+    # The grouping schedule's actions ("VC-Attention" Sec. 3.4, App. A): a warm-started regroup with half
+    # the rounds, pi kept with new means, pi kept without means; amortised over the pages' 40-step run.
+    vc.vc_attn_prepare(Q, K, V, cfg["k"], cfg["iters"], plan=plan)
+    warm_iters = max(1, cfg["iters"] // 2)
+    t_step = {
+        vc.VC_STEP_GROUP: t_prep_full,
+        vc.VC_STEP_GROUP_WARM: time_it(lambda: vc.vc_attn_prepare_ex(
+            Q, K, V, cfg["k"], warm_iters, flags=vc.STEP_PREPARE_FLAGS[vc.VC_STEP_GROUP_WARM], plan=plan)),
+        vc.VC_STEP_REUSE: time_it(lambda: vc.vc_attn_prepare_ex(
+            Q, K, V, cfg["k"], cfg["iters"], flags=vc.STEP_PREPARE_FLAGS[vc.VC_STEP_REUSE], plan=plan)),
+        vc.VC_STEP_PLAIN: time_it(lambda: vc.vc_attn_prepare_ex(
+            Q, K, V, cfg["k"], cfg["iters"], flags=vc.STEP_PREPARE_FLAGS[vc.VC_STEP_PLAIN], plan=plan)),
+    }
+    n_sched = 40
+    sched_prepare_ms = sum(t_step[vc.vc_schedule_action(s_, n_sched, 4)] for s_ in range(n_sched)) / n_sched
     vc.vc_attn_prepare(Q, K, V, cfg["k"], cfg["iters"], plan=plan)
     torch.cuda.synchronize()
 
@@ -350,6 +365,11 @@ def main():
         "pct_fp8_peak": 100.0 * fwd_tflops / fp8_peak,
         "prepare_ms": t_prep_full, "prepare_quant_ms": t_prep_quant, "grouping_ms": t_group,
         "amortised_prepare_ms": t_prep_quant + 3.0 / 40.0 * t_group,
+        "schedule": {"steps": 40, "reuse": 4, "warm_iters": warm_iters,
+                     "prepare_ms_per_action": {"group": t_step[vc.VC_STEP_GROUP],
+                                               "group_warm": t_step[vc.VC_STEP_GROUP_WARM],
+                                               "reuse": t_step[vc.VC_STEP_REUSE], "plain": t_step[vc.VC_STEP_PLAIN]},
+                     "prepare_ms_per_step": sched_prepare_ms},
         "roofline": {"bound": "tensor", "kernel": "vc_fwd_kernel<128>", "achieved": fwd_tflops, "peak": fp8_peak,
                      "unit": "TFLOP/s", "frac": fwd_tflops / fp8_peak, "traffic": profiled_traffic(cfg),
                      "peak_source": f"{src} bf16 burst {bf16_burst:.0f} TFLOP/s x {FP8_OVER_BF16:.0f} (FP8/BF16 nominal)"},

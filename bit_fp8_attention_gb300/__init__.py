@@ -30,6 +30,8 @@ VC_EXPCAST = 1
 VC_VSMOOTH = 2
 VC_MIDWINDOW = 4
 VC_KCENTER = 8
+VC_WARM_START = 16
+VC_REUSE_PERM = 32
 VC_DEBUG_TIMEOUT = 1 << 16
 VC_FLAGS_DEFAULT = VC_EXPCAST | VC_VSMOOTH | VC_MIDWINDOW
 
@@ -45,9 +47,11 @@ VC_PLAN_MEANS = 9
 VC_PLAN_CENTROIDS = 10
 VC_PLAN_KCENTER = 11
 VC_NOALLOC_MAX_HEADS = 4096
+VC_STEP_GROUP, VC_STEP_GROUP_WARM, VC_STEP_REUSE, VC_STEP_PLAIN = 0, 1, 2, 3
 
 EXPORTS = ("vc_attn_prepare", "vc_attn_prepare_ex", "vc_attn_forward", "vc_plan_size", "vc_plan_get",
-           "vc_plan_status", "vc_plan_shape", "vc_plan_destroy", "vc_expcast_encode", "vc_strerror", "vc_version")
+           "vc_plan_status", "vc_plan_shape", "vc_plan_destroy", "vc_expcast_encode", "vc_schedule_action",
+           "vc_strerror", "vc_version")
 
 
 class VCError(RuntimeError):
@@ -79,6 +83,7 @@ def lib() -> ctypes.CDLL:
         "vc_plan_destroy": (None, [vp]),
         "vc_expcast_encode": (i, [vp, vp, vp, ctypes.c_int64, vp, vp]),
         "vc_residual_pack_noalloc": (i, [vp, vp, i, i, i, i, vp, vp, vp, vp]),
+        "vc_schedule_action": (i, [i, i, i]),
         "vc_strerror": (ctypes.c_char_p, [i]),
         "vc_version": (ctypes.c_char_p, []),
     }
@@ -101,6 +106,19 @@ def _stream(stream) -> int:
 def _check(rc: int, what: str):
     if rc != VC_OK:
         raise VCError(rc, what)
+
+
+def vc_schedule_action(step: int, n_steps: int, reuse: int = 4) -> int:
+    """VC_STEP_* action of a denoising step (see include/vc_attn.h); raises on invalid arguments."""
+    rc = lib().vc_schedule_action(step, n_steps, reuse)
+    if rc < 0:
+        raise VCError(rc, "vc_schedule_action")
+    return rc
+
+
+# Prepare flags of each schedule action (include/vc_attn.h, grouping schedule).
+STEP_PREPARE_FLAGS = {VC_STEP_GROUP: VC_VSMOOTH, VC_STEP_GROUP_WARM: VC_VSMOOTH | VC_WARM_START,
+                      VC_STEP_REUSE: VC_VSMOOTH | VC_REUSE_PERM, VC_STEP_PLAIN: VC_REUSE_PERM}
 
 
 def vc_strerror(rc: int) -> str:

@@ -131,8 +131,15 @@ int vc_attn_prepare_ex(const void* Q, const void* K, const void* V, int B, int H
   int rc = check_shape(B, H, S, D, k_clusters);
   if (rc != VC_OK) return rc;
   const bool vsmooth = (flags & VC_VSMOOTH) != 0;
-  const bool grouping = vsmooth && !perm;
+  const bool reuse_perm = (flags & VC_REUSE_PERM) != 0;
+  const bool grouping = vsmooth && !perm && !reuse_perm;
+  const bool warm = grouping && (flags & VC_WARM_START) != 0;
   if (grouping && (iters < 1 || iters > kMaxIters)) return VC_ERR_INVALID_ARG;
+  if (reuse_perm && perm) return VC_ERR_INVALID_ARG;
+  // A warm start needs the centroids of an earlier grouping, a reuse the permutation of an earlier
+  // prepare: both only on an existing plan.
+  if ((warm && !(*plan && (*plan)->b.has_grouping)) || (reuse_perm && !(*plan && (*plan)->b.has_perm)))
+    return VC_ERR_INVALID_ARG;
   rc = check_device();
   if (rc != VC_OK) return rc;
   if (*plan) {
@@ -145,8 +152,13 @@ int vc_attn_prepare_ex(const void* Q, const void* K, const void* V, int B, int H
   vc_plan* pl = *plan;
   pl->b.has_means = vsmooth;
   pl->b.has_kcenter = (flags & VC_KCENTER) != 0;
-  return vc::prepare_launch(pl->b, (const uint16_t*)Q, (const uint16_t*)K, (const uint16_t*)V,
-                            vsmooth ? perm : nullptr, vsmooth, pl->b.has_kcenter, iters, stream);
+  rc = vc::prepare_launch(pl->b, (const uint16_t*)Q, (const uint16_t*)K, (const uint16_t*)V,
+                          vsmooth ? perm : nullptr, vsmooth, pl->b.has_kcenter, reuse_perm, warm, iters, stream);
+  if (rc == VC_OK) {
+    if (grouping) pl->b.has_grouping = true;
+    pl->b.has_perm = true;
+  }
+  return rc;
 }
 
 int vc_attn_prepare(const void* Q, const void* K, const void* V, int B, int H, int S, int D, int k_clusters,
@@ -253,6 +265,14 @@ const char* vc_strerror(int status) {
     case VC_ERR_NO_DEVICE: return "no sm_103 device";
     default: return "unknown status";
   }
+}
+
+int vc_schedule_action(int step, int n_steps, int reuse) {
+  if (n_steps < 1 || reuse < 1 || step < 0 || step >= n_steps) return VC_ERR_INVALID_ARG;
+  const int window = (n_steps + 3) / 4;  // the first 25% of the steps, rounded up
+  if (step >= window) return VC_STEP_PLAIN;
+  if (step % reuse != 0) return VC_STEP_REUSE;
+  return step == 0 ? VC_STEP_GROUP : VC_STEP_GROUP_WARM;
 }
 
 const char* vc_version(void) { return "vc_attn 0.1.0 (sm_103a)"; }

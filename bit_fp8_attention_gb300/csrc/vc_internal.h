@@ -35,15 +35,20 @@ struct PlanBuffers {
   unsigned long long* ksum;  // [BH, D] exact fixed-point channel sums of K
   uint16_t* kmu;        // [BH, D] bf16 channel centre of K
   bool has_kcenter;     // prepared with K centering
+  bool has_grouping;    // the centroids hold a finished grouping (a warm start may begin from them)
+  bool has_perm;        // pi holds a permutation from an earlier prepare
   unsigned int* vamax;  // [BH] residual |max| as float bits
   int* status;          // [1]
   bool has_means;       // prepared with V-Smooth
 };
 
+// perm_in: a caller permutation to copy in; reuse_perm: keep the plan's pi (no k-means); otherwise
+// with vsmooth, k-means (warm: from the plan's centroids).  Means only with vsmooth.
 int prepare_launch(const PlanBuffers& p, const uint16_t* Q, const uint16_t* K, const uint16_t* V,
-                   const int32_t* perm_in, bool vsmooth, bool kcenter, int iters, cudaStream_t st);
+                   const int32_t* perm_in, bool vsmooth, bool kcenter, bool reuse_perm, bool warm, int iters,
+                   cudaStream_t st);
 
-int kmeans_launch(const PlanBuffers& p, const uint16_t* V, int iters, cudaStream_t st);
+int kmeans_launch(const PlanBuffers& p, const uint16_t* V, int iters, bool warm, cudaStream_t st);
 int kmeans_chunks(int S);
 
 // cuTensorMapEncodeTiled on a 2-D row-major tensor (rows x inner elements, row pitch in bytes).

@@ -471,7 +471,7 @@ __global__ void __launch_bounds__(256) kmeans_update_kernel(const uint16_t* __re
 }
 
 template <int D>
-int launch_kmeans(const PlanBuffers& p, const uint16_t* V, int iters, cudaStream_t st) {
+int launch_kmeans(const PlanBuffers& p, const uint16_t* V, int iters, bool warm, cudaStream_t st) {
   using C = AsgCfg<D>;
   const int BH = p.B * p.H, S = p.S, k = p.k, kpad = p.kpad;
   static bool attr_set = false;
@@ -491,7 +491,8 @@ int launch_kmeans(const PlanBuffers& p, const uint16_t* V, int iters, cudaStream
   const dim3 gc((kpad + 7) / 8, BH), gu((k + 7) / 8, BH);
   const dim3 ga((S + C::TPC * 128 - 1) / (C::TPC * 128), BH);
   const dim3 gh(p.nchunk, BH);
-  kmeans_init_kernel<D><<<gc, 256, 0, st>>>(V, S, k, kpad, p.cent, p.cnorm, p.cent16, p.cnormp);
+  // Warm start: the centroids of the plan's previous grouping (and their splits and norms) stay.
+  if (!warm) kmeans_init_kernel<D><<<gc, 256, 0, st>>>(V, S, k, kpad, p.cent, p.cnorm, p.cent16, p.cnormp);
   for (int it = 0; it < iters; ++it) {
     kmeans_assign_kernel<D><<<ga, 320, C::SMEM, st>>>(xmap, cmap, p.cnormp, S, kpad, p.labels, p.status);
     label_hist_kernel<<<gh, 256, 0, st>>>(p.labels, S, k, p.nchunk, p.chist);
@@ -505,8 +506,8 @@ int launch_kmeans(const PlanBuffers& p, const uint16_t* V, int iters, cudaStream
 
 }  // namespace
 
-int kmeans_launch(const PlanBuffers& p, const uint16_t* V, int iters, cudaStream_t st) {
-  return p.D == 128 ? launch_kmeans<128>(p, V, iters, st) : launch_kmeans<64>(p, V, iters, st);
+int kmeans_launch(const PlanBuffers& p, const uint16_t* V, int iters, bool warm, cudaStream_t st) {
+  return p.D == 128 ? launch_kmeans<128>(p, V, iters, warm, st) : launch_kmeans<64>(p, V, iters, warm, st);
 }
 
 int kmeans_chunks(int S) { return (S + kChunk - 1) / kChunk; }

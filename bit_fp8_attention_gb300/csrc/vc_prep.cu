@@ -321,7 +321,8 @@ __global__ void __launch_bounds__(256) vpack_kernel(const uint16_t* __restrict__
 static int check_launch() { return cudaPeekAtLastError() == cudaSuccess ? 0 : VC_ERR_CUDA; }
 
 int prepare_launch(const PlanBuffers& p, const uint16_t* Q, const uint16_t* K, const uint16_t* V,
-                   const int32_t* perm_in, bool vsmooth, bool kcenter, int iters, cudaStream_t st) {
+                   const int32_t* perm_in, bool vsmooth, bool kcenter, bool reuse_perm, bool warm, int iters,
+                   cudaStream_t st) {
   const int BH = p.B * p.H, S = p.S, D = p.D, nkb = p.nkb, S_pad = p.S_pad;
   dim3 gblk(nkb, BH);
   // Q: per-block quantisation in token order
@@ -329,13 +330,15 @@ int prepare_launch(const PlanBuffers& p, const uint16_t* Q, const uint16_t* K, c
   else quant_blocks_kernel<64><<<gblk, 256, 0, st>>>(Q, nullptr, nullptr, S, S_pad, p.qcodes, p.qscales);
   if (check_launch()) return VC_ERR_CUDA;
   const int32_t* perm = nullptr;
-  if (vsmooth) {
+  if (reuse_perm) {  // the permutation of an earlier prepare stays (grouping schedule)
+    perm = p.perm;
+  } else if (vsmooth) {
     if (perm_in) {
       if (cudaMemcpyAsync(p.perm, perm_in, sizeof(int32_t) * (size_t)BH * S, cudaMemcpyDeviceToDevice, st) !=
           cudaSuccess)
         return VC_ERR_CUDA;
     } else {
-      int rc = kmeans_launch(p, V, iters, st);
+      int rc = kmeans_launch(p, V, iters, warm, st);
       if (rc != VC_OK) return rc;
     }
     perm = p.perm;

@@ -64,6 +64,16 @@ enum {
      key has the head's channel mean mu (bf16 of the exact mean over the S tokens) subtracted in fp32
      before its block quantisation; the softmax is unchanged, the keys' quantisation range shrinks. */
   VC_KCENTER = 8u,
+  /* Prepare only: begin the k-means rounds from the plan's centroids of its previous grouping
+     instead of the rows floor(i*S/k) (VC-Attention Sec. 3.2 "Unbalanced clusters cost little":
+     warm-starting from the previous step's centroids halves the grouping cost). Needs a plan that
+     has been grouped before (else VC_ERR_INVALID_ARG); ignored when no k-means runs. */
+  VC_WARM_START = 16u,
+  /* Prepare only: keep the plan's permutation from an earlier prepare, no k-means (the grouping
+     schedule's reuse steps). With VC_VSMOOTH the block means are recomputed on the new V; without it
+     the permutation is kept and no means are used ("the plain low-bit kernel on the permutation the
+     window left behind"). Needs a plan prepared before; not with an explicit perm. */
+  VC_REUSE_PERM = 32u,
   /* Test hook: the forward kernel's first internal wait gives up at once, so the call reports
      VC_ERR_TIMEOUT through vc_plan_status() without hanging. */
   VC_DEBUG_TIMEOUT = 1u << 16
@@ -176,6 +186,20 @@ int vc_expcast_encode(const float* s, const float* a, const float* b, int64_t n,
 #define VC_NOALLOC_MAX_HEADS 4096
 int vc_residual_pack_noalloc(const void* V, const int32_t* perm, int B, int H, int S, int D, void* means,
                              uint8_t* vcodes, float* vscales, cudaStream_t stream);
+
+/* ---- grouping schedule ------------------------------------------------------------------ */
+/* What a denoising step of an n_steps run does (VC-Attention Sec. 3.4 "Amortized grouping schedule",
+ * App. A "Grouping schedule"): grouping and demeaning run on the first ceil(n_steps/4) steps; inside
+ * that window the permutation is computed at every `reuse`-th step (the pages use 4: steps 0, 4, 8 of
+ * a 40-step run) and reused in between; later steps run the plain kernel on the kept permutation.
+ * Returns a VC_STEP_* value, or VC_ERR_INVALID_ARG for step outside [0, n_steps), n_steps < 1 or
+ * reuse < 1.  Pure host logic: needs no device.  Prepare flags per action:
+ *   VC_STEP_GROUP      VC_VSMOOTH                  (k-means from scratch)
+ *   VC_STEP_GROUP_WARM VC_VSMOOTH | VC_WARM_START  (from the previous centroids, fewer rounds)
+ *   VC_STEP_REUSE      VC_VSMOOTH | VC_REUSE_PERM  (same pi, new means)
+ *   VC_STEP_PLAIN      VC_REUSE_PERM               (same pi, no means) */
+enum { VC_STEP_GROUP = 0, VC_STEP_GROUP_WARM = 1, VC_STEP_REUSE = 2, VC_STEP_PLAIN = 3 };
+int vc_schedule_action(int step, int n_steps, int reuse);
 
 /* Human-readable text of a status code (static storage). */
 const char* vc_strerror(int status);

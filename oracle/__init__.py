@@ -71,6 +71,8 @@ def lib():
             "orc_expcast_of_u": (ctypes.c_int, [ctypes.c_double]),
             "orc_quant_blocks": (None, [u16, ctypes.c_int64, ctypes.c_int, u8, f32]),
             "orc_quant_blocks_centered": (None, [u16, ctypes.c_int64, ctypes.c_int, u16, u8, f32]),
+            "orc_kmeans_from": (None, [u16, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, i32, f64, f64]),
+            "orc_schedule_action": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
             "orc_channel_mean_bf16": (None, [u16, ctypes.c_int64, ctypes.c_int, u16]),
             "orc_kmeans_objective": (ctypes.c_double, [u16, ctypes.c_int64, ctypes.c_int, ctypes.c_int, i32]),
             "orc_kmeans": (None, [u16, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, i32, f64, f64]),
@@ -215,19 +217,35 @@ def channel_mean_bf16(x) -> np.ndarray:
     return mu
 
 
-def kmeans(v, k: int, iters: int):
+def kmeans(v, k: int, iters: int, init=None):
     """Lloyd k-means over value tokens ([VC] §3.2 "Value-guided permutation", "Unbalanced clusters").
 
+    init: None (centroid i starts as row floor(i*S/k)), or [k, D] starting centroids (warm start from a
+    previous grouping, "Unbalanced clusters cost little").
     Returns labels [S] int32, centroids [k, D] float64, objective of each round [iters].
     """
     v = _u16(v)
     S, D = v.shape
     labels = np.empty(S, dtype=np.int32)
-    cent = np.empty((k, D), dtype=np.float64)
     J = np.empty(max(iters, 1), dtype=np.float64)
-    lib().orc_kmeans(_ptr(v, ctypes.c_uint16), S, D, k, iters, _ptr(labels, ctypes.c_int32),
-                     _ptr(cent, ctypes.c_double), _ptr(J, ctypes.c_double))
+    if init is None:
+        cent = np.empty((k, D), dtype=np.float64)
+        lib().orc_kmeans(_ptr(v, ctypes.c_uint16), S, D, k, iters, _ptr(labels, ctypes.c_int32),
+                         _ptr(cent, ctypes.c_double), _ptr(J, ctypes.c_double))
+    else:
+        cent = np.array(init, dtype=np.float64, copy=True).reshape(k, D)
+        lib().orc_kmeans_from(_ptr(v, ctypes.c_uint16), S, D, k, iters, _ptr(labels, ctypes.c_int32),
+                              _ptr(cent, ctypes.c_double), _ptr(J, ctypes.c_double))
     return labels, cent, J[:iters]
+
+
+GROUP, GROUP_WARM, REUSE, PLAIN = 0, 1, 2, 3
+
+
+def schedule_action(step: int, n_steps: int, reuse: int = 4) -> int:
+    """Grouping schedule ([VC] §3.4 "Amortized grouping schedule", App. A "Grouping schedule"):
+    GROUP / GROUP_WARM / REUSE / PLAIN for one denoising step."""
+    return int(lib().orc_schedule_action(step, n_steps, reuse))
 
 
 def kmeans_objective(v, k: int, labels) -> float:

@@ -225,12 +225,11 @@ double orc_kmeans_objective(const uint16_t* v, int64_t S, int D, int k, const in
   return J;
 }
 
-void orc_kmeans(const uint16_t* v, int64_t S, int D, int k, int iters, int32_t* labels, double* centroids,
-                double* J_rounds) {
-  for (int i = 0; i < k; ++i) {
-    int64_t src = (int64_t)((double)i * (double)S / (double)k);
-    for (int d = 0; d < D; ++d) centroids[(int64_t)i * D + d] = bf16_to_f32(v[src * D + d]);
-  }
+/* Lloyd rounds from the centroids already in `centroids` ([k, D], fp64).  Warm start ([VC] §3.2
+ * "Unbalanced clusters cost little": "warm-starting each step from the previous step's centroids
+ * halves its cost"): the caller passes the previous grouping's centroids here instead of rows. */
+void orc_kmeans_from(const uint16_t* v, int64_t S, int D, int k, int iters, int32_t* labels, double* centroids,
+                     double* J_rounds) {
   double* sum = (double*)malloc((size_t)k * D * sizeof(double));
   int64_t* cnt = (int64_t*)malloc((size_t)k * sizeof(int64_t));
   for (int it = 0; it < iters; ++it) {
@@ -264,6 +263,31 @@ void orc_kmeans(const uint16_t* v, int64_t S, int D, int k, int iters, int32_t* 
   }
   free(sum);
   free(cnt);
+}
+
+void orc_kmeans(const uint16_t* v, int64_t S, int D, int k, int iters, int32_t* labels, double* centroids,
+                double* J_rounds) {
+  for (int i = 0; i < k; ++i) {
+    int64_t src = (int64_t)((double)i * (double)S / (double)k);
+    for (int d = 0; d < D; ++d) centroids[(int64_t)i * D + d] = bf16_to_f32(v[src * D + d]);
+  }
+  orc_kmeans_from(v, S, D, k, iters, labels, centroids, J_rounds);
+}
+
+/* ---------------------------------------------------------------------------------------------
+ * Grouping schedule over a run of n denoising steps.  [VC] §3.4 "Amortized grouping schedule" and
+ * App. A "Grouping schedule": grouping and demeaning run on the first 25% of the steps, a window of
+ * ceil(n/4) steps; inside it the permutation is computed once and reused for `reuse` adjacent steps
+ * (4 in the pages: steps 0, 4, 8 of a 40-step run); after the window the plain low-bit kernel runs on
+ * the permutation the window left behind (reading R12: pi kept, no means).
+ * Returns 0 = group from scratch, 1 = group warm-started from the previous centroids, 2 = reuse pi
+ * with V-Smooth, 3 = plain kernel on the kept pi.
+ * ------------------------------------------------------------------------------------------- */
+int orc_schedule_action(int step, int n_steps, int reuse) {
+  const int window = (n_steps + 3) / 4;
+  if (step >= window) return 3;
+  if (step % reuse != 0) return 2;
+  return step == 0 ? 0 : 1;
 }
 
 /* Stable argsort of the labels by counting sort: pi lists the tokens of cluster 0 in token order,

@@ -69,6 +69,10 @@ def test_invalid_arguments_rejected_without_device(L):
     # non-positive sizes, grouping without iterations
     assert L.vc_attn_prepare(fake, fake, fake, 0, 1, 128, 128, 1, 1, None, ctypes.byref(plan)) == -1
     assert L.vc_attn_prepare(fake, fake, fake, 1, 1, 128, 128, 1, 0, None, ctypes.byref(plan)) == -1
+    # a warm start or a permutation reuse needs a plan that has been grouped / prepared before
+    assert L.vc_attn_prepare_ex(fake, fake, fake, 1, 1, 128, 128, 1, 2, None, 2 | 16, None, ctypes.byref(plan)) == -1
+    assert L.vc_attn_prepare_ex(fake, fake, fake, 1, 1, 128, 128, 1, 2, None, 2 | 32, None, ctypes.byref(plan)) == -1
+    assert L.vc_attn_prepare_ex(fake, fake, fake, 1, 1, 128, 128, 1, 2, fake, 2 | 32, None, ctypes.byref(plan)) == -1
     assert plan.value is None
     # forward / plan calls on a null plan
     assert L.vc_attn_forward(None, fake, 7, None) == -1
