@@ -78,11 +78,15 @@ def lib():
             "orc_kmeans": (None, [u16, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, i32, f64, f64]),
             "orc_stable_argsort": (None, [i32, ctypes.c_int64, ctypes.c_int, i32]),
             "orc_demean": (None, [u16, i32, ctypes.c_int64, ctypes.c_int, ctypes.c_int, f64, u16, f32, u8, f32, f32]),
+            "orc_demean_ex": (None, [u16, i32, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, f64, u16, u16,
+                                     f32, u8, f32, f32]),
             "orc_gather_rows": (None, [u16, i32, ctypes.c_int64, ctypes.c_int, u16]),
             "orc_visit_order": (None, [ctypes.c_int, ctypes.c_int, ctypes.c_int, i32]),
             "orc_code_scale": (ctypes.c_float, [ctypes.c_int]),
             "orc_attention_quant": (None, [u8, f32, u8, f32, u8, ctypes.c_float, u16, ctypes.c_int64, ctypes.c_int,
                                            ctypes.c_int, i64, ctypes.c_int64, f64, f64, f32]),
+            "orc_attention_quant_ex": (None, [u8, f32, u8, f32, u8, ctypes.c_float, f32, u16, u16, ctypes.c_int64,
+                                              ctypes.c_int, ctypes.c_int, i64, ctypes.c_int64, f64, f64, f32]),
             "orc_attention_exact": (None, [u16, u16, u16, ctypes.c_int64, ctypes.c_int, i64, ctypes.c_int64, f64]),
             "orc_attention_demeaned_exact": (None, [f64, f64, f64, ctypes.c_int64, ctypes.c_int, ctypes.c_int, i64,
                                                     ctypes.c_int64, f64]),
@@ -273,10 +277,12 @@ def gather_rows(x, perm) -> np.ndarray:
     return out
 
 
-def demean(v, perm=None, subtract_mean: bool = True) -> dict:
-    """Gather by pi, 128-row block means, residual and its per-head E4M3 quantisation.
+def demean(v, perm=None, subtract_mean: bool = True, per_channel: bool = False) -> dict:
+    """Gather by pi, 128-row block means, residual and its E4M3 quantisation.
 
-    [VC] §3.2 "Block demeaning" Eq. 4; [OVC] one V scale per head.
+    [VC] §3.2 "Block demeaning" Eq. 4. per_channel=False: one V scale per head ([OVC]); "amax" and
+    "sv" are floats. per_channel=True: one scale per channel ([VC] §3.2, App. B); "amax" and "sv" are
+    [D] float32 arrays and "mut" holds the means divided by the channel scales (bf16 bits).
     """
     v = _u16(v)
     S, D = v.shape
@@ -284,14 +290,21 @@ def demean(v, perm=None, subtract_mean: bool = True) -> dict:
     p = None if perm is None else np.ascontiguousarray(np.asarray(perm, dtype=np.int32))
     mu = np.empty((nkb, D), dtype=np.float64)
     mub = np.empty((nkb, D), dtype=np.uint16)
+    mut = np.zeros((nkb, D), dtype=np.uint16)
     resid = np.empty((nkb * BLOCK, D), dtype=np.float32)
     rc = np.empty((nkb * BLOCK, D), dtype=np.uint8)
-    amax = ctypes.c_float()
-    sv = ctypes.c_float()
-    lib().orc_demean(_ptr(v, ctypes.c_uint16), None if p is None else _ptr(p, ctypes.c_int32), S, D,
-                     1 if subtract_mean else 0, _ptr(mu, ctypes.c_double), _ptr(mub, ctypes.c_uint16),
-                     _ptr(resid, ctypes.c_float), _ptr(rc, ctypes.c_uint8), ctypes.byref(amax), ctypes.byref(sv))
-    return {"mu": mu, "mub": mub, "resid": resid, "rc": rc, "amax": float(amax.value), "sv": float(sv.value)}
+    amax = np.zeros(D, dtype=np.float32)
+    sv = np.zeros(D, dtype=np.float32)
+    lib().orc_demean_ex(_ptr(v, ctypes.c_uint16), None if p is None else _ptr(p, ctypes.c_int32), S, D,
+                        1 if subtract_mean else 0, 1 if per_channel else 0, _ptr(mu, ctypes.c_double),
+                        _ptr(mub, ctypes.c_uint16), _ptr(mut, ctypes.c_uint16), _ptr(resid, ctypes.c_float),
+                        _ptr(rc, ctypes.c_uint8), _ptr(amax, ctypes.c_float), _ptr(sv, ctypes.c_float))
+    out = {"mu": mu, "mub": mub, "resid": resid, "rc": rc}
+    if per_channel:
+        out.update(amax=amax, sv=sv, mut=mut)
+    else:
+        out.update(amax=float(amax[0]), sv=float(sv[0]))
+    return out
 
 
 def visit_order(nkb: int, qt: int, midwindow: bool = True) -> np.ndarray:
@@ -304,10 +317,12 @@ def visit_order(nkb: int, qt: int, midwindow: bool = True) -> np.ndarray:
 # ----------------------------------------------------------------------------------------------
 # Attention
 # ----------------------------------------------------------------------------------------------
-def attention_quant(qc, sq, kc, sk, rc, sv: float, mub, S: int, rows, flags: int = EXPCAST | MIDWINDOW):
+def attention_quant(qc, sq, kc, sk, rc, sv, mub, S: int, rows, flags: int = EXPCAST | MIDWINDOW, mut=None):
     """(i) The quantised forward for the given query rows of one batch-head.
 
     [VC] §3.1 Eq. 1, §3.2 Eq. 6, §3.3 Eq. 7; [OVC] true-score max, consistent denominator, order.
+    sv is a float (one residual scale per head; mub the means) or a [D] array of per-channel scales,
+    then with mut the means divided by them ([VC] App. B).
     Returns (out [n, D] fp64 = sv*A/l, l [n], M [n] float32 final running max in code units).
     """
     qc = np.ascontiguousarray(qc, dtype=np.uint8)
@@ -321,12 +336,22 @@ def attention_quant(qc, sq, kc, sk, rc, sv: float, mub, S: int, rows, flags: int
     out = np.empty((n, D), dtype=np.float64)
     l = np.empty(n, dtype=np.float64)
     m = np.empty(n, dtype=np.float32)
+    svc = None
+    if np.ndim(sv) > 0:
+        svc = np.ascontiguousarray(sv, dtype=np.float32)
+        assert svc.shape == (D,)
+        sv = 1.0
     mub_keep = None if mub is None else np.ascontiguousarray(mub, dtype=np.uint16)
-    mu_p = None if mub_keep is None else _ptr(mub_keep, ctypes.c_uint16)
-    lib().orc_attention_quant(_ptr(qc, ctypes.c_uint8), _ptr(sq, ctypes.c_float), _ptr(kc, ctypes.c_uint8),
-                              _ptr(sk, ctypes.c_float), _ptr(rc, ctypes.c_uint8), sv, mu_p, S, D, flags,
-                              _ptr(rows, ctypes.c_int64), n, _ptr(out, ctypes.c_double), _ptr(l, ctypes.c_double),
-                              _ptr(m, ctypes.c_float))
+    mut_keep = None if mut is None else np.ascontiguousarray(mut, dtype=np.uint16)
+    if svc is not None and mub_keep is not None:
+        assert mut_keep is not None, "per-channel scales need the scaled means"
+    lib().orc_attention_quant_ex(_ptr(qc, ctypes.c_uint8), _ptr(sq, ctypes.c_float), _ptr(kc, ctypes.c_uint8),
+                                 _ptr(sk, ctypes.c_float), _ptr(rc, ctypes.c_uint8), float(sv),
+                                 None if svc is None else _ptr(svc, ctypes.c_float),
+                                 None if mub_keep is None else _ptr(mub_keep, ctypes.c_uint16),
+                                 None if (svc is None or mut_keep is None) else _ptr(mut_keep, ctypes.c_uint16),
+                                 S, D, flags, _ptr(rows, ctypes.c_int64), n, _ptr(out, ctypes.c_double),
+                                 _ptr(l, ctypes.c_double), _ptr(m, ctypes.c_float))
     return out, l, m
 
 
@@ -359,12 +384,13 @@ def attention_demeaned_exact(q, k, v, rows, midwindow: bool = True) -> np.ndarra
 # Whole-path conveniences for one batch-head
 # ----------------------------------------------------------------------------------------------
 def prepare_head(q, k, v, k_clusters: int, iters: int, vsmooth: bool = True, perm=None,
-                 kcenter: bool = False) -> dict:
+                 kcenter: bool = False, vscale_channel: bool = False) -> dict:
     """Everything the prepare step produces for one batch-head, computed on the CPU.
 
     vsmooth=False: identity permutation, no means (R = V). perm given: use it instead of k-means
     (the parity tests feed the GPU's permutation here, as the acceptance rule says).
     kcenter: subtract the keys' channel mean before their quantisation (see channel_mean_bf16).
+    vscale_channel: one residual scale per channel instead of one per head (see demean).
     """
     q, k, v = _u16(q), _u16(k), _u16(v)
     S, D = q.shape
@@ -383,9 +409,11 @@ def prepare_head(q, k, v, k_clusters: int, iters: int, vsmooth: bool = True, per
     kmu = channel_mean_bf16(k) if kcenter else None
     out["kmu"] = kmu
     out["kc"], out["sk"] = quant_blocks(kp, center=kmu)
-    dm = demean(v, perm, subtract_mean=vsmooth)
-    out.update(rc=dm["rc"], sv=dm["sv"], amax=dm["amax"], mub=dm["mub"], mu=dm["mu"], resid=dm["resid"])
+    dm = demean(v, perm, subtract_mean=vsmooth, per_channel=vscale_channel)
+    out.update(rc=dm["rc"], sv=dm["sv"], amax=dm["amax"], mub=dm["mub"], mu=dm["mu"], resid=dm["resid"],
+               mut=dm.get("mut"))
     out["vsmooth"] = vsmooth
+    out["vscale_channel"] = vscale_channel
     return out
 
 
@@ -393,7 +421,7 @@ def forward_head(prep: dict, rows, expcast: bool = True, midwindow: bool = True)
     flags = (EXPCAST if expcast else 0) | (MIDWINDOW if midwindow else 0)
     mub = prep["mub"] if prep["vsmooth"] else None
     return attention_quant(prep["qc"], prep["sq"], prep["kc"], prep["sk"], prep["rc"], prep["sv"], mub,
-                           prep["S"], rows, flags)
+                           prep["S"], rows, flags, mut=prep.get("mut") if prep["vsmooth"] else None)
 
 
 def num_threads() -> int:

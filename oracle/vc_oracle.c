@@ -27,6 +27,10 @@
  *   R7  Key visit order for query tile qt: start = min(nkb-1, 2*floor(qt/2) + 2), sweep down to 0, then
  *       the tail. The two query tiles 2m and 2m+1 share one order (2 and 1 blocks past their
  *       diagonals), so that one pass over the keys can serve both.
+ *   R17 Per-channel V residual scale (an option; one scale per head is the default): the channel's
+ *       scale is its residual amax over the whole head / 448 (1 when the channel is all zero), and
+ *       the stored block means are bf16(fp32(mean) / scale), so that the single epilogue multiply
+ *       by the channel's scale restores both the residual and the mean term.
  */
 #include <math.h>
 #include <stdint.h>
@@ -309,12 +313,19 @@ void orc_stable_argsort(const int32_t* z, int64_t S, int k, int32_t* perm) {
  * Outputs: mu [nkb, D] fp64 (exact mean), mub [nkb, D] bf16 bits, resid [S_pad, D] fp32 (pad rows
  * zero), rcodes [S_pad, D] E4M3 codes of R * 448/amax, *amax_out, *sv_out = amax/448.
  * ------------------------------------------------------------------------------------------- */
-void orc_demean(const uint16_t* v, const int32_t* perm, int64_t S, int D, int subtract_mean, double* mu,
-                uint16_t* mub, float* resid, uint8_t* rcodes, float* amax_out, float* sv_out) {
+/* per_channel = 0: one residual scale per head ([OVC]); amax_out[0], sv_out[0] and mut unused.
+ * per_channel = 1: one scale per channel ([VC] §3.2 "Block demeaning": the residual goes through
+ * "per-channel E4M3 at 8 bits"; App. B: "the means are stored divided by the per-channel value
+ * scale, so the kernel's single epilogue multiply applies to both terms of Eq. 6").  Reading R17:
+ * amax_out[d] = max_t |R[t,d]| over the head, sv_out[d] = amax_d/448 (1 for an all-zero channel),
+ * codes E4M3(R * (448/amax_d)), and the stored means mut[j,d] = bf16(fp32(mub[j,d]) / sv[d]). */
+void orc_demean_ex(const uint16_t* v, const int32_t* perm, int64_t S, int D, int subtract_mean, int per_channel,
+                   double* mu, uint16_t* mub, uint16_t* mut, float* resid, uint8_t* rcodes, float* amax_out,
+                   float* sv_out) {
   int64_t nkb = (S + ORC_BLOCK - 1) / ORC_BLOCK;
   memset(resid, 0, (size_t)(nkb * ORC_BLOCK * D) * sizeof(float));
   memset(rcodes, 0, (size_t)(nkb * ORC_BLOCK * D));
-  float amax = 0.0f;
+  float* amax = (float*)calloc((size_t)D, sizeof(float));
   for (int64_t j = 0; j < nkb; ++j) {
     int64_t t0 = j * ORC_BLOCK, t1 = t0 + ORC_BLOCK < S ? t0 + ORC_BLOCK : S;
     for (int d = 0; d < D; ++d) {
@@ -332,16 +343,32 @@ void orc_demean(const uint16_t* v, const int32_t* perm, int64_t S, int D, int su
       for (int d = 0; d < D; ++d) {
         float r = bf16_to_f32(v[src * D + d]) - bf16_to_f32(mub[j * D + d]);
         resid[t * D + d] = r;
-        if (fabsf(r) > amax) amax = fabsf(r);
+        if (fabsf(r) > amax[d]) amax[d] = fabsf(r);
       }
     }
   }
-  float inv = amax > 0.0f ? 448.0f / amax : 1.0f;
-  float sv = amax > 0.0f ? amax / 448.0f : 1.0f;
-  for (int64_t t = 0; t < S; ++t)
-    for (int d = 0; d < D; ++d) rcodes[t * D + d] = orc_e4m3_encode(resid[t * D + d] * inv);
-  *amax_out = amax;
-  *sv_out = sv;
+  if (!per_channel) {  /* one scale over the whole head */
+    float a = 0.0f;
+    for (int d = 0; d < D; ++d) a = amax[d] > a ? amax[d] : a;
+    for (int d = 0; d < D; ++d) amax[d] = a;
+  }
+  for (int d = 0; d < D; ++d) {
+    float inv = amax[d] > 0.0f ? 448.0f / amax[d] : 1.0f;
+    for (int64_t t = 0; t < S; ++t) rcodes[t * D + d] = orc_e4m3_encode(resid[t * D + d] * inv);
+  }
+  for (int d = 0; d < (per_channel ? D : 1); ++d) {
+    amax_out[d] = amax[d];
+    sv_out[d] = amax[d] > 0.0f ? amax[d] / 448.0f : 1.0f;
+  }
+  if (per_channel && mut)
+    for (int64_t j = 0; j < nkb; ++j)
+      for (int d = 0; d < D; ++d) mut[j * D + d] = orc_f64_to_bf16((double)(bf16_to_f32(mub[j * D + d]) / sv_out[d]));
+  free(amax);
+}
+
+void orc_demean(const uint16_t* v, const int32_t* perm, int64_t S, int D, int subtract_mean, double* mu,
+                uint16_t* mub, float* resid, uint8_t* rcodes, float* amax_out, float* sv_out) {
+  orc_demean_ex(v, perm, S, D, subtract_mean, 0, mu, mub, NULL, resid, rcodes, amax_out, sv_out);
 }
 
 /* Gather rows of a [S, D] bf16 tensor by pi: out[t] = x[pi[t]]  ([VC] §3.2 Eq. 3: K' = K[pi]). */
@@ -383,9 +410,12 @@ void orc_visit_order(int nkb, int qt, int midwindow, int32_t* order) {
 
 float orc_code_scale(int D) { return (float)(8.0 * 1.4426950408889634 / sqrt((double)D)); }
 
-void orc_attention_quant(const uint8_t* qc, const float* sq, const uint8_t* kc, const float* sk, const uint8_t* rc,
-                         float sv, const uint16_t* mub, int64_t S, int D, int flags, const int64_t* rows,
-                         int64_t nrows, double* out, double* l_out, float* m_out) {
+/* svc: NULL (one residual scale sv per head, means mub in true units) or [D] per-channel scales with mut
+ * the means already divided by them (R17): then the mean term is r_j * mut[j,d] and O[d] = svc[d] A[d] / l. */
+void orc_attention_quant_ex(const uint8_t* qc, const float* sq, const uint8_t* kc, const float* sk,
+                            const uint8_t* rc, float sv, const float* svc, const uint16_t* mub, const uint16_t* mut,
+                            int64_t S, int D, int flags, const int64_t* rows, int64_t nrows, double* out,
+                            double* l_out, float* m_out) {
   int nkb = (int)((S + ORC_BLOCK - 1) / ORC_BLOCK);
   float C = orc_code_scale(D);
 #pragma omp parallel
@@ -442,12 +472,14 @@ void orc_attention_quant(const uint8_t* qc, const float* sq, const uint8_t* kc, 
           double acc = 0.0;
           for (int c = 0; c < ncols; ++c)
             acc += orc_e4m3_decode(code[c]) * orc_e4m3_decode(rc[((int64_t)j * ORC_BLOCK + c) * D + d]);
-          double mean_term = mub ? rj * ((double)bf16_to_f32(mub[(int64_t)j * D + d]) / (double)sv) : 0.0;
+          double mean_term = 0.0;
+          if (mub && svc && mut) mean_term = rj * (double)bf16_to_f32(mut[(int64_t)j * D + d]);
+          else if (mub) mean_term = rj * ((double)bf16_to_f32(mub[(int64_t)j * D + d]) / (double)sv);
           A[d] += acc + mean_term;
         }
         l += rj;
       }
-      for (int d = 0; d < D; ++d) out[ri * D + d] = (double)sv * A[d] / l;
+      for (int d = 0; d < D; ++d) out[ri * D + d] = (double)(svc ? svc[d] : sv) * A[d] / l;
       if (l_out) l_out[ri] = l;
       if (m_out) m_out[ri] = M;
     }
@@ -455,6 +487,12 @@ void orc_attention_quant(const uint8_t* qc, const float* sq, const uint8_t* kc, 
     free(A);
     free(qd);
   }
+}
+
+void orc_attention_quant(const uint8_t* qc, const float* sq, const uint8_t* kc, const float* sk, const uint8_t* rc,
+                         float sv, const uint16_t* mub, int64_t S, int D, int flags, const int64_t* rows,
+                         int64_t nrows, double* out, double* l_out, float* m_out) {
+  orc_attention_quant_ex(qc, sq, kc, sk, rc, sv, NULL, mub, NULL, S, D, flags, rows, nrows, out, l_out, m_out);
 }
 
 /* ---------------------------------------------------------------------------------------------
