@@ -32,6 +32,7 @@ VC_MIDWINDOW = 4
 VC_KCENTER = 8
 VC_WARM_START = 16
 VC_REUSE_PERM = 32
+VC_VSCALE_CHANNEL = 64
 VC_DEBUG_TIMEOUT = 1 << 16
 VC_FLAGS_DEFAULT = VC_EXPCAST | VC_VSMOOTH | VC_MIDWINDOW
 
@@ -46,6 +47,8 @@ VC_PLAN_VSCALES = 8
 VC_PLAN_MEANS = 9
 VC_PLAN_CENTROIDS = 10
 VC_PLAN_KCENTER = 11
+VC_PLAN_VCHSCALES = 12
+VC_PLAN_MEANS_T = 13
 VC_NOALLOC_MAX_HEADS = 4096
 VC_STEP_GROUP, VC_STEP_GROUP_WARM, VC_STEP_REUSE, VC_STEP_PLAIN = 0, 1, 2, 3
 
@@ -208,6 +211,8 @@ _PLAN_DTYPES = {
     VC_PLAN_MEANS: (torch.bfloat16, lambda p: (p.B, p.H, p.nkb, p.D)),
     VC_PLAN_CENTROIDS: (torch.float32, lambda p: (p.B, p.H, p.k, p.D)),
     VC_PLAN_KCENTER: (torch.bfloat16, lambda p: (p.B, p.H, p.D)),
+    VC_PLAN_VCHSCALES: (torch.float32, lambda p: (p.B, p.H, p.D)),
+    VC_PLAN_MEANS_T: (torch.bfloat16, lambda p: (p.B, p.H, p.D, (p.nkb + 15) // 16 * 16)),
 }
 
 

@@ -81,6 +81,8 @@ int plan_create(int B, int H, int S, int D, int k, vc_plan** out) {
       BH * D * 8,                     // ksum
       BH * D * 2,                     // kmu
       BH * 4,                         // vamax
+      BH * D * 4,                     // vamax_ch
+      BH * D * 4,                     // vscales_ch
       16,                             // status
   };
   size_t total = 0;
@@ -97,7 +99,7 @@ int plan_create(int B, int H, int S, int D, int k, vc_plan** out) {
                     (void**)&b.perm,   (void**)&b.cent,    (void**)&b.cnorm,   (void**)&b.counts,
                     (void**)&b.offsets, (void**)&b.cent16, (void**)&b.cnormp,  (void**)&b.chist,
                     (void**)&b.kexp,   (void**)&b.ksum,    (void**)&b.kmu,
-                    (void**)&b.vamax,  (void**)&b.status};
+                    (void**)&b.vamax,  (void**)&b.vamax_ch, (void**)&b.vscales_ch, (void**)&b.status};
   for (size_t i = 0; i < sizeof(sizes) / sizeof(sizes[0]); ++i) {
     *slots[i] = p;
     p += align_up(sizes[i]);
@@ -152,8 +154,10 @@ int vc_attn_prepare_ex(const void* Q, const void* K, const void* V, int B, int H
   vc_plan* pl = *plan;
   pl->b.has_means = vsmooth;
   pl->b.has_kcenter = (flags & VC_KCENTER) != 0;
+  pl->b.has_vchannel = (flags & VC_VSCALE_CHANNEL) != 0;
   rc = vc::prepare_launch(pl->b, (const uint16_t*)Q, (const uint16_t*)K, (const uint16_t*)V,
-                          vsmooth ? perm : nullptr, vsmooth, pl->b.has_kcenter, reuse_perm, warm, iters, stream);
+                          vsmooth ? perm : nullptr, vsmooth, pl->b.has_kcenter, reuse_perm, warm,
+                          pl->b.has_vchannel, iters, stream);
   if (rc == VC_OK) {
     if (grouping) pl->b.has_grouping = true;
     pl->b.has_perm = true;
@@ -189,6 +193,8 @@ size_t vc_plan_size(const vc_plan* plan, int what) {
     case VC_PLAN_MEANS: return BH * b.nkb * b.D * 2;
     case VC_PLAN_CENTROIDS: return BH * b.k * b.D * 4;
     case VC_PLAN_KCENTER: return BH * b.D * 2;
+    case VC_PLAN_VCHSCALES: return BH * b.D * 4;
+    case VC_PLAN_MEANS_T: return BH * b.D * b.nkb16 * 2;
     default: return 0;
   }
 }
@@ -210,6 +216,8 @@ int vc_plan_get(const vc_plan* plan, int what, void* dst, size_t bytes, cudaStre
     case VC_PLAN_MEANS: src = b.means; break;
     case VC_PLAN_CENTROIDS: src = b.cent; break;
     case VC_PLAN_KCENTER: src = b.kmu; break;
+    case VC_PLAN_VCHSCALES: src = b.vscales_ch; break;
+    case VC_PLAN_MEANS_T: src = b.meansT; break;
   }
   return cudaMemcpyAsync(dst, src, n, cudaMemcpyDefault, stream) == cudaSuccess ? VC_OK : VC_ERR_CUDA;
 }

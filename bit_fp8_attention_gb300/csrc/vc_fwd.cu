@@ -73,6 +73,7 @@ struct FwdArgs {
   const float* qscales;
   const float* kscales;
   const float* vscales;
+  const float* vscales_ch;  // [BH, D] per-channel residual scales, or null (one scale per head)
   uint16_t* out;
   int* status;
   int S, S_pad, nkb;
@@ -472,8 +473,11 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
     const uint32_t tP = tmem + lane_base + (wg ? C::T_P1 : C::T_P0);
     const float* skh = args.kscales + (int64_t)bh * nkb;
     const float aq = args.code_scale * args.qscales[(int64_t)bh * nkb + qt];
+    // One scale per head: the means are in true units and the flush operand carries 1/sV. Per
+    // channel: the means are already divided by the channel scales, and the epilogue applies them.
+    const float* svch = args.vscales_ch ? args.vscales_ch + (int64_t)bh * D : nullptr;
     const float sv = args.vscales[bh];
-    const float inv_sv = 1.f / sv;
+    const float inv_sv = svch ? 1.f : 1.f / sv;
     const int tail_valid = args.S - (nkb - 1) * 128;
     bool ok = true;
     int known = -1;  // every PV up to this tile is known complete
@@ -652,7 +656,8 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
       mbar_arrive(&p_full[wg]);
     }
 
-    // Group 0 finishes: every PV done, the last run's row sums and means, then O = sV A / l.
+    // Group 0 finishes: every PV done, the last run's row sums and means, then O = sV A / l (with
+    // per-channel scales O[:, d] = s_d A[:, d] / l).
     if (wg == 0 && ok && !warp_aborted(abort_flag) && ensure_pv(nkb - 1)) {
       float w[16];
       read_w(w);
@@ -671,7 +676,7 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
         tc_fence_after();
       }
       if (ready) {
-        const float scale = sv / l;
+        const float scale = svch ? 1.f / l : sv / l;
         const int64_t qrow = (int64_t)qt * 128 + row;
         uint16_t* orow = args.out + ((int64_t)bh * args.S + qrow) * D;
 #pragma unroll 1
@@ -682,8 +687,12 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
           uint32_t packed[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            __nv_bfloat162 h2 =
-                __floats2bfloat162_rn(__uint_as_float(o[2 * i]) * scale, __uint_as_float(o[2 * i + 1]) * scale);
+            float x0 = __uint_as_float(o[2 * i]), x1 = __uint_as_float(o[2 * i + 1]);
+            if (svch) {
+              x0 *= __ldg(svch + c0 + 2 * i);
+              x1 *= __ldg(svch + c0 + 2 * i + 1);
+            }
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(x0 * scale, x1 * scale);
             packed[i] = *reinterpret_cast<uint32_t*>(&h2);
           }
           if (qrow < args.S) {
@@ -764,6 +773,7 @@ static int launch_fwd(const PlanBuffers& p, const FwdMaps& maps, uint16_t* O, un
   a.qscales = p.qscales;
   a.kscales = p.kscales;
   a.vscales = p.vscales;
+  a.vscales_ch = p.has_vchannel ? p.vscales_ch : nullptr;
   a.out = O;
   a.status = p.status;
   a.S = p.S;

@@ -38,6 +38,9 @@ struct PlanBuffers {
   bool has_grouping;    // the centroids hold a finished grouping (a warm start may begin from them)
   bool has_perm;        // pi holds a permutation from an earlier prepare
   unsigned int* vamax;  // [BH] residual |max| as float bits
+  unsigned int* vamax_ch;  // [BH, D] residual |max| of each channel as float bits (per-channel scale)
+  float* vscales_ch;    // [BH, D] residual scale of each channel
+  bool has_vchannel;    // prepared with one residual scale per channel
   int* status;          // [1]
   bool has_means;       // prepared with V-Smooth
 };
@@ -45,8 +48,8 @@ struct PlanBuffers {
 // perm_in: a caller permutation to copy in; reuse_perm: keep the plan's pi (no k-means); otherwise
 // with vsmooth, k-means (warm: from the plan's centroids).  Means only with vsmooth.
 int prepare_launch(const PlanBuffers& p, const uint16_t* Q, const uint16_t* K, const uint16_t* V,
-                   const int32_t* perm_in, bool vsmooth, bool kcenter, bool reuse_perm, bool warm, int iters,
-                   cudaStream_t st);
+                   const int32_t* perm_in, bool vsmooth, bool kcenter, bool reuse_perm, bool warm, bool vchannel,
+                   int iters, cudaStream_t st);
 
 int kmeans_launch(const PlanBuffers& p, const uint16_t* V, int iters, bool warm, cudaStream_t st);
 int kmeans_chunks(int S);

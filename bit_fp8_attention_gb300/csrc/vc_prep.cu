@@ -195,12 +195,14 @@ __global__ void iota_kernel(int32_t* __restrict__ perm, int S, int64_t total) {
 // integer M * 2^(E - E_max + 45) (|sum| < 2^60 in int64), exact whenever the column spans at most 45
 // binades. Whenever an fp64 running sum would be exact too (a span of at most 38 binades), the double
 // (sum * 2^(E_max - 179)) / n_j is then the same double, and so is the bf16 mean. R = V' - mu_b in
-// fp32; amax_h = max |R| over the head (atomicMax on the bit pattern of a non-negative float).
+// fp32; amax_h = max |R| over the head (atomicMax on the bit pattern of a non-negative float) and,
+// when amax_ch is given, amax_d = max |R[:, d]| of every channel over the head the same way.
 template <int D>
 __global__ void __launch_bounds__(256) vmeans_kernel(const uint16_t* __restrict__ v, const int32_t* __restrict__ perm,
                                                      int S, int demean, uint16_t* __restrict__ mub,
                                                      unsigned int* __restrict__ amax_bits,
-                                                     uint16_t* __restrict__ mubT = nullptr, int nkb16 = 0) {
+                                                     uint16_t* __restrict__ mubT = nullptr, int nkb16 = 0,
+                                                     unsigned int* __restrict__ amax_ch = nullptr) {
   constexpr int SPLIT = 256 / D;  // threads per column
   const int j = blockIdx.x, bh = blockIdx.y;
   const int nkb = (S + 127) / 128;
@@ -213,6 +215,7 @@ __global__ void __launch_bounds__(256) vmeans_kernel(const uint16_t* __restrict_
   __shared__ long long sums[SPLIT][D];
   __shared__ float mus[D];
   __shared__ float red[8];
+  __shared__ float cmax[SPLIT][D];
   constexpr int CPR = D / 8;  // 16-byte chunks per row
   for (int c = threadIdx.x; c < n * CPR; c += 256) {
     const int r = c / CPR, cc = c % CPR;
@@ -254,6 +257,16 @@ __global__ void __launch_bounds__(256) vmeans_kernel(const uint16_t* __restrict_
     float res = __fsub_rn(bf16_bits_to_f32(blk[r][d]), mus[d]);
     amax = fmaxf(amax, fabsf(res));
   }
+  if (amax_ch) {  // per channel: combine the column's parts, one atomic per channel
+    cmax[part][d] = amax;
+    __syncthreads();
+    if (part == 0) {
+      float m = cmax[0][d];
+#pragma unroll
+      for (int q = 1; q < SPLIT; ++q) m = fmaxf(m, cmax[q][d]);
+      atomicMax(amax_ch + (int64_t)bh * D + d, __float_as_uint(m));
+    }
+  }
   for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
   __syncthreads();
@@ -264,15 +277,21 @@ __global__ void __launch_bounds__(256) vmeans_kernel(const uint16_t* __restrict_
   }
 }
 
-// Residual codes, transposed: Vt[bh][d][t] = E4M3(R[t][d] * 448/amax_h), t < S_pad (pad = 0).
+// Residual codes, transposed: Vt[bh][d][t] = E4M3(R[t][d] * 448/amax), t < S_pad (pad = 0), with
+// amax the head's (amax_h) or, when amax_ch is given, the channel's (amax_d).
 // One CTA per (block, bh): the block's rows are gathered into shared memory with 16-byte loads, then
 // each thread codes 32 rows of one channel (reads along the channels are conflict-free) and writes
-// them as one 32-byte sector of the transposed output.
+// them as one 32-byte sector of the transposed output.  The first block's CTA writes the scales
+// (svc: the scale of every channel, equal to the head's without amax_ch).  With amax_ch the
+// transposed means the forward reads become bf16(mu / s_d), one correctly rounded fp32 division.
 template <int D>
 __global__ void __launch_bounds__(256) vpack_kernel(const uint16_t* __restrict__ v, const int32_t* __restrict__ perm,
                                                     int S, int S_pad, const uint16_t* __restrict__ mub,
                                                     const unsigned int* __restrict__ amax_bits,
-                                                    uint8_t* __restrict__ vt, float* __restrict__ sv) {
+                                                    uint8_t* __restrict__ vt, float* __restrict__ sv,
+                                                    const unsigned int* __restrict__ amax_ch = nullptr,
+                                                    float* __restrict__ svc = nullptr,
+                                                    uint16_t* __restrict__ mubT = nullptr, int nkb16 = 0) {
   const int j = blockIdx.x, bh = blockIdx.y;
   const int nkb = S_pad / 128;
   const int t0 = j * 128, n = min(128, S - t0);
@@ -280,22 +299,38 @@ __global__ void __launch_bounds__(256) vpack_kernel(const uint16_t* __restrict__
   const int32_t* ph = perm ? perm + (int64_t)bh * S : nullptr;
   __shared__ __align__(16) uint16_t blk[128][D];
   __shared__ float mus[D];
+  __shared__ float invs[D];
   const float amax = __uint_as_float(amax_bits[bh]);
   const bool zero = !(amax > 0.f);
-  const float inv = zero ? 1.f : __fdiv_rn(448.f, amax);
-  if (j == 0 && threadIdx.x == 0) sv[bh] = zero ? 1.f : __fdiv_rn(amax, 448.f);
+  const float inv_h = zero ? 1.f : __fdiv_rn(448.f, amax);
+  const float sv_h = zero ? 1.f : __fdiv_rn(amax, 448.f);
+  if (j == 0 && threadIdx.x == 0) sv[bh] = sv_h;
+  for (int d = threadIdx.x; d < D; d += 256) {
+    const float mu = bf16_bits_to_f32(mub[((int64_t)bh * nkb + j) * D + d]);
+    mus[d] = mu;
+    if (amax_ch) {
+      const float a = __uint_as_float(amax_ch[(int64_t)bh * D + d]);
+      const bool z = !(a > 0.f);
+      const float s_d = z ? 1.f : __fdiv_rn(a, 448.f);
+      invs[d] = z ? 1.f : __fdiv_rn(448.f, a);
+      if (j == 0) svc[(int64_t)bh * D + d] = s_d;
+      mubT[((int64_t)bh * D + d) * nkb16 + j] = f64_to_bf16_rne((double)__fdiv_rn(mu, s_d));
+    } else {
+      invs[d] = inv_h;
+      if (j == 0 && svc) svc[(int64_t)bh * D + d] = sv_h;
+    }
+  }
   constexpr int CPR = D / 8;  // 16-byte chunks per row
   for (int c = threadIdx.x; c < n * CPR; c += 256) {
     const int r = c / CPR, cc = c % CPR;
     const int src = ph ? ph[t0 + r] : t0 + r;
     *reinterpret_cast<uint4*>(&blk[r][cc * 8]) = __ldg(reinterpret_cast<const uint4*>(vh + (int64_t)src * D) + cc);
   }
-  for (int d = threadIdx.x; d < D; d += 256) mus[d] = bf16_bits_to_f32(mub[((int64_t)bh * nkb + j) * D + d]);
   __syncthreads();
   uint8_t* out = vt + (int64_t)bh * D * S_pad + (int64_t)t0;
   for (int task = threadIdx.x; task < D * 4; task += 256) {
     const int d = task % D, seg = task / D;  // rows [32 seg, 32 seg + 32) of channel d
-    const float mu = mus[d];
+    const float mu = mus[d], inv = invs[d];
     uint32_t w[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
@@ -321,8 +356,8 @@ __global__ void __launch_bounds__(256) vpack_kernel(const uint16_t* __restrict__
 static int check_launch() { return cudaPeekAtLastError() == cudaSuccess ? 0 : VC_ERR_CUDA; }
 
 int prepare_launch(const PlanBuffers& p, const uint16_t* Q, const uint16_t* K, const uint16_t* V,
-                   const int32_t* perm_in, bool vsmooth, bool kcenter, bool reuse_perm, bool warm, int iters,
-                   cudaStream_t st) {
+                   const int32_t* perm_in, bool vsmooth, bool kcenter, bool reuse_perm, bool warm, bool vchannel,
+                   int iters, cudaStream_t st) {
   const int BH = p.B * p.H, S = p.S, D = p.D, nkb = p.nkb, S_pad = p.S_pad;
   dim3 gblk(nkb, BH);
   // Q: per-block quantisation in token order
@@ -367,12 +402,17 @@ int prepare_launch(const PlanBuffers& p, const uint16_t* Q, const uint16_t* K, c
   else quant_blocks_kernel<64><<<gblk, 256, 0, st>>>(K, perm, kcen, S, S_pad, p.kcodes, p.kscales);
   // V' = V[pi]: block means, residual maximum per head, residual codes transposed
   if (cudaMemsetAsync(p.vamax, 0, sizeof(unsigned int) * BH, st) != cudaSuccess) return VC_ERR_CUDA;
+  unsigned int* ach = vchannel ? p.vamax_ch : nullptr;
+  if (vchannel && cudaMemsetAsync(p.vamax_ch, 0, sizeof(unsigned int) * (size_t)BH * D, st) != cudaSuccess)
+    return VC_ERR_CUDA;
   if (D == 128) {
-    vmeans_kernel<128><<<gblk, 256, 0, st>>>(V, perm, S, vsmooth ? 1 : 0, p.means, p.vamax, p.meansT, p.nkb16);
-    vpack_kernel<128><<<gblk, 256, 0, st>>>(V, perm, S, S_pad, p.means, p.vamax, p.vcodes, p.vscales);
+    vmeans_kernel<128><<<gblk, 256, 0, st>>>(V, perm, S, vsmooth ? 1 : 0, p.means, p.vamax, p.meansT, p.nkb16, ach);
+    vpack_kernel<128><<<gblk, 256, 0, st>>>(V, perm, S, S_pad, p.means, p.vamax, p.vcodes, p.vscales, ach,
+                                            p.vscales_ch, p.meansT, p.nkb16);
   } else {
-    vmeans_kernel<64><<<gblk, 256, 0, st>>>(V, perm, S, vsmooth ? 1 : 0, p.means, p.vamax, p.meansT, p.nkb16);
-    vpack_kernel<64><<<gblk, 256, 0, st>>>(V, perm, S, S_pad, p.means, p.vamax, p.vcodes, p.vscales);
+    vmeans_kernel<64><<<gblk, 256, 0, st>>>(V, perm, S, vsmooth ? 1 : 0, p.means, p.vamax, p.meansT, p.nkb16, ach);
+    vpack_kernel<64><<<gblk, 256, 0, st>>>(V, perm, S, S_pad, p.means, p.vamax, p.vcodes, p.vscales, ach,
+                                           p.vscales_ch, p.meansT, p.nkb16);
   }
   return check_launch();
 }

@@ -74,6 +74,13 @@ enum {
      the permutation is kept and no means are used ("the plain low-bit kernel on the permutation the
      window left behind"). Needs a plan prepared before; not with an explicit perm. */
   VC_REUSE_PERM = 32u,
+  /* Prepare only: one residual scale per channel instead of one per head (VC-Attention Sec. 3.2
+     "Block demeaning": the residual is quantised per channel to E4M3; App. B: the block means the
+     forward reads are stored divided by the channel scale, so one multiply per channel in the
+     epilogue restores both terms of Eq. 6).  s_d = max_t |R[t, d]| / 448 over the head (1 for an
+     all-zero channel); codes E4M3(R[t, d] * (448 / amax_d)); forward means bf16(mu / s_d).  The
+     forward then computes O[:, d] = s_d * A[:, d] / l. */
+  VC_VSCALE_CHANNEL = 64u,
   /* Test hook: the forward kernel's first internal wait gives up at once, so the call reports
      VC_ERR_TIMEOUT through vc_plan_status() without hanging. */
   VC_DEBUG_TIMEOUT = 1u << 16
@@ -112,7 +119,8 @@ int vc_attn_prepare(const void* Q, const void* K, const void* V, int B, int H, i
  *   schedule"; it is not checked to be a permutation -- every entry must lie in [0, S)).
  * flags: VC_VSMOOTH set -> group (unless perm is given) and demean; clear -> identity
  *   permutation (perm ignored), no means, R = V.  VC_KCENTER set -> subtract the keys' channel
- *   centre before their quantisation.  Other bits are ignored here. */
+ *   centre before their quantisation.  VC_VSCALE_CHANNEL set -> one residual scale per channel.
+ *   VC_WARM_START / VC_REUSE_PERM as documented with the flags.  Other bits are ignored here. */
 int vc_attn_prepare_ex(const void* Q, const void* K, const void* V, int B, int H, int S, int D, int k_clusters,
                        int iters, const int32_t* perm, unsigned flags, cudaStream_t stream, vc_plan** plan);
 
@@ -123,7 +131,8 @@ int vc_attn_prepare_ex(const void* Q, const void* K, const void* V, int B, int H
  * becomes an E4M3 code c = clip[0,120](rne(S*a_j + 119.65 - M)) with a_j = 8 log2(e)/sqrt(D)
  * * sQ * sK_j (or the exp-then-cast path without VC_EXPCAST); the codes multiply the residual
  * codes of V' on FP8 tensor cores; the row sum of the decoded codes (the denominator) and the
- * block means (VC_VSMOOTH) enter the accumulator; O = sV * A / l in bf16.
+ * block means (VC_VSMOOTH) enter the accumulator; O = sV * A / l in bf16 (per channel,
+ * O[:, d] = s_d * A[:, d] / l, when the plan was prepared with VC_VSCALE_CHANNEL).
  * plan: from vc_attn_prepare.  O: device bf16 [B, H, S, D], rows in the original token order.
  * flags: VC_EXPCAST | VC_MIDWINDOW | VC_VSMOOTH (VC_VSMOOTH is ignored when the plan was
  * prepared without means) | VC_DEBUG_TIMEOUT.  Kernel-side timeouts are reported
@@ -139,10 +148,17 @@ enum {
   VC_PLAN_KCODES = 5,    /* uint8 [B, H, S_pad, D] E4M3 codes of K' = K[pi]                  */
   VC_PLAN_KSCALES = 6,   /* fp32  [B, H, nkb]                                                 */
   VC_PLAN_VCODES = 7,    /* uint8 [B, H, D, S_pad] E4M3 codes of the residual, transposed     */
-  VC_PLAN_VSCALES = 8,   /* fp32  [B, H]           per-head residual scale                    */
+  VC_PLAN_VSCALES = 8,   /* fp32  [B, H]           per-head residual scale (with
+                                                     VC_VSCALE_CHANNEL: the largest channel scale) */
   VC_PLAN_MEANS = 9,     /* bf16  [B, H, nkb, D]   block means of V'                          */
   VC_PLAN_CENTROIDS = 10, /* fp32 [B, H, k, D]     centroids after the last update           */
-  VC_PLAN_KCENTER = 11   /* bf16  [B, H, D]        K channel centre (prepared with VC_KCENTER) */
+  VC_PLAN_KCENTER = 11,  /* bf16  [B, H, D]        K channel centre (prepared with VC_KCENTER) */
+  VC_PLAN_VCHSCALES = 12, /* fp32 [B, H, D]        the residual scale of each channel (all equal
+                                                     to the head's scale without VC_VSCALE_CHANNEL) */
+  VC_PLAN_MEANS_T = 13   /* bf16  [B, H, D, nkb16] the means as the forward reads them: transposed,
+                                                     nkb16 = 16*ceil(nkb/16) with zero pad columns,
+                                                     divided by the channel scale with
+                                                     VC_VSCALE_CHANNEL, else in true units         */
 };
 /* Size in bytes of one plan tensor (0 for an unknown `what` or a NULL plan). */
 size_t vc_plan_size(const vc_plan* plan, int what);

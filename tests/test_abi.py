@@ -45,6 +45,19 @@ def test_python_binding_names_match_abi():
         assert hasattr(vc, name), name
 
 
+def test_python_constants_match_header():
+    """Every flag, plan-tensor id, error code and step action the header defines has the same value
+    in the binding."""
+    import bit_fp8_attention_gb300 as vc
+
+    text = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "vc_attn.h")).read(), flags=re.S)
+    consts = re.findall(r"\b(VC_[A-Z0-9_]+)\s*=\s*(-?\d+)u?(?:\s*<<\s*(\d+))?", text)
+    assert len(consts) >= 30
+    for name, val, sh in consts:
+        want = int(val) << int(sh) if sh else int(val)
+        assert getattr(vc, name) == want, name
+
+
 def test_strerror_and_version(L):
     import bit_fp8_attention_gb300 as vc
 

@@ -252,3 +252,65 @@ def test_k_centering(m, S, D):
         rel_f, _ = errors(got, oracle_forward_from_plan(g, S, rows))
         assert rel_f <= FWD_ONLY_REL, f"head {h}: forward-only rel-L2 {rel_f:.3e}"
     plan.destroy()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("S,D,vsmooth", [(3000, 64, True), (2049, 128, True), (1000, 128, False)])
+def test_per_channel_v_scale(m, S, D, vsmooth):
+    """VC_VSCALE_CHANNEL ("VC-Attention", Sec. 3.2 "Block demeaning", App. B): values with a few outlier
+    channels 2^12 wider than the rest. Channel scales, residual codes and the scaled means the forward
+    reads are bit-exact against the oracle fed the GPU's permutation; the forward meets the acceptance
+    rule on every channel separately (max-abs against that channel's own max |V|)."""
+    cfg = synth.custom(S, D=D, H=2, k=max(1, S // 128), iters=2)
+    Q, K, V = synth.make_inputs(cfg, seed=21, device="cuda")
+    gen = torch.Generator().manual_seed(22)
+    wide = torch.randperm(D, generator=gen)[:3]
+    gain = torch.ones(D)
+    gain[wide] = 4096.0
+    V = (V.float() * gain.cuda()).to(torch.bfloat16).contiguous()
+    flags = (m.VC_VSMOOTH if vsmooth else 0) | m.VC_VSCALE_CHANNEL
+    plan = m.vc_attn_prepare_ex(Q, K, V, cfg["k"], cfg["iters"], flags=flags)
+    O = m.vc_attn_forward(plan)
+    assert m.vc_plan_status(plan) == (0, 0)
+    allp = gpu_plan_all(m, plan)
+    svc = m.vc_plan_get(plan, m.VC_PLAN_VCHSCALES).cpu().numpy()
+    mt = u16(m.vc_plan_get(plan, m.VC_PLAN_MEANS_T))
+    nkb = (S + 127) // 128
+    rows = np.arange(S)
+    for h in range(2):
+        g = head_of(allp, 0, h)
+        o = oracle.prepare_head(u16(Q[0, h]), u16(K[0, h]), u16(V[0, h]), cfg["k"], cfg["iters"],
+                                vsmooth=vsmooth, perm=g["perm"] if vsmooth else None, vscale_channel=True)
+        assert np.array_equal(svc[0, h], o["sv"]), f"head {h}: channel scales"
+        assert g["sv"] == np.float32(o["sv"].max()), f"head {h}: head scale"
+        assert np.array_equal(g["rc"], o["rc"]), f"head {h}: residual codes"
+        assert np.array_equal(g["mub"], o["mub"]), f"head {h}: block means"
+        for key in ("qc", "sq", "kc", "sk"):
+            assert np.array_equal(g[key], o[key]), f"head {h}: {key}"
+        assert np.array_equal(mt[0, h, :, :nkb].T, o["mut"]), f"head {h}: scaled means"
+        assert not mt[0, h, :, nkb:].any()
+        ref, _, _ = oracle.forward_head(o, rows)
+        got = f64(O[0, h])
+        Vh = np.abs(f64(V[0, h]))
+        for d in range(D):
+            rel, mx = errors(got[:, d], ref[:, d])
+            assert rel <= 1e-2 and mx <= 3e-2 * Vh[:, d].max(), f"head {h} channel {d}: rel {rel:.3e} max {mx:.3e}"
+        fwd = oracle.attention_quant(g["qc"], g["sq"], g["kc"], g["sk"], g["rc"], svc[0, h], g["mub"] if vsmooth
+                                     else None, S, rows, mut=mt[0, h, :, :nkb].T if vsmooth else None)[0]
+        rel_f, _ = errors(got, fwd)
+        assert rel_f <= FWD_ONLY_REL, f"head {h}: forward-only rel-L2 {rel_f:.3e}"
+    plan.destroy()
+
+
+@pytest.mark.gpu
+def test_per_head_plan_reports_equal_channel_scales(m):
+    cfg = synth.custom(700, D=64, H=1, k=5, iters=2)
+    Q, K, V = synth.make_inputs(cfg, seed=23, device="cuda")
+    plan = m.vc_attn_prepare(Q, K, V, cfg["k"], cfg["iters"])
+    sv = m.vc_plan_get(plan, m.VC_PLAN_VSCALES).cpu().numpy()
+    svc = m.vc_plan_get(plan, m.VC_PLAN_VCHSCALES).cpu().numpy()
+    assert np.array_equal(svc[0, 0], np.full(64, sv[0, 0], dtype=np.float32))
+    mt = u16(m.vc_plan_get(plan, m.VC_PLAN_MEANS_T))
+    mub = u16(m.vc_plan_get(plan, m.VC_PLAN_MEANS))
+    assert np.array_equal(mt[0, 0, :, :6].T, mub[0, 0])  # true units without per-channel scales
+    plan.destroy()
