@@ -87,6 +87,10 @@ def lib():
                                            ctypes.c_int, i64, ctypes.c_int64, f64, f64, f32]),
             "orc_attention_quant_ex": (None, [u8, f32, u8, f32, u8, ctypes.c_float, f32, u16, u16, ctypes.c_int64,
                                               ctypes.c_int, ctypes.c_int, i64, ctypes.c_int64, f64, f64, f32]),
+            "orc_repair_select": (None, [u16, ctypes.c_int64, ctypes.c_int, f32, ctypes.c_int64, i32, f32, u8]),
+            "orc_attention_quant_rep": (None, [u8, f32, u8, f32, u8, ctypes.c_float, f32, u16, u16, u8, f32, u8,
+                                               ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int, i64,
+                                               ctypes.c_int64, f64, f64, f32]),
             "orc_attention_exact": (None, [u16, u16, u16, ctypes.c_int64, ctypes.c_int, i64, ctypes.c_int64, f64]),
             "orc_attention_demeaned_exact": (None, [f64, f64, f64, ctypes.c_int64, ctypes.c_int, ctypes.c_int, i64,
                                                     ctypes.c_int64, f64]),
@@ -317,12 +321,14 @@ def visit_order(nkb: int, qt: int, midwindow: bool = True) -> np.ndarray:
 # ----------------------------------------------------------------------------------------------
 # Attention
 # ----------------------------------------------------------------------------------------------
-def attention_quant(qc, sq, kc, sk, rc, sv, mub, S: int, rows, flags: int = EXPCAST | MIDWINDOW, mut=None):
+def attention_quant(qc, sq, kc, sk, rc, sv, mub, S: int, rows, flags: int = EXPCAST | MIDWINDOW, mut=None,
+                    repair=None):
     """(i) The quantised forward for the given query rows of one batch-head.
 
     [VC] §3.1 Eq. 1, §3.2 Eq. 6, §3.3 Eq. 7; [OVC] true-score max, consistent denominator, order.
     sv is a float (one residual scale per head; mub the means) or a [D] array of per-channel scales,
-    then with mut the means divided by them ([VC] App. B).
+    then with mut the means divided by them ([VC] App. B). repair: None or the dict repair_rows()
+    returns ([OVC] V residual repair: numerator-only rows visited last).
     Returns (out [n, D] fp64 = sv*A/l, l [n], M [n] float32 final running max in code units).
     """
     qc = np.ascontiguousarray(qc, dtype=np.uint8)
@@ -345,14 +351,57 @@ def attention_quant(qc, sq, kc, sk, rc, sv, mub, S: int, rows, flags: int = EXPC
     mut_keep = None if mut is None else np.ascontiguousarray(mut, dtype=np.uint16)
     if svc is not None and mub_keep is not None:
         assert mut_keep is not None, "per-channel scales need the scaled means"
-    lib().orc_attention_quant_ex(_ptr(qc, ctypes.c_uint8), _ptr(sq, ctypes.c_float), _ptr(kc, ctypes.c_uint8),
-                                 _ptr(sk, ctypes.c_float), _ptr(rc, ctypes.c_uint8), float(sv),
-                                 None if svc is None else _ptr(svc, ctypes.c_float),
-                                 None if mub_keep is None else _ptr(mub_keep, ctypes.c_uint16),
-                                 None if (svc is None or mut_keep is None) else _ptr(mut_keep, ctypes.c_uint16),
-                                 S, D, flags, _ptr(rows, ctypes.c_int64), n, _ptr(out, ctypes.c_double),
-                                 _ptr(l, ctypes.c_double), _ptr(m, ctypes.c_float))
+    n_rep = 0
+    kr = sr = rr = None
+    if repair is not None and repair["n"] > 0:
+        n_rep = int(repair["n"])
+        kr = np.ascontiguousarray(repair["kc"], dtype=np.uint8)
+        sr = np.ascontiguousarray(repair["sk"], dtype=np.float32)
+        rr = np.ascontiguousarray(repair["rc"], dtype=np.uint8)
+        assert kr.shape == rr.shape == (nkb_of(n_rep) * BLOCK, D) and sr.shape == (nkb_of(n_rep),)
+    lib().orc_attention_quant_rep(_ptr(qc, ctypes.c_uint8), _ptr(sq, ctypes.c_float), _ptr(kc, ctypes.c_uint8),
+                                  _ptr(sk, ctypes.c_float), _ptr(rc, ctypes.c_uint8), float(sv),
+                                  None if svc is None else _ptr(svc, ctypes.c_float),
+                                  None if mub_keep is None else _ptr(mub_keep, ctypes.c_uint16),
+                                  None if (svc is None or mut_keep is None) else _ptr(mut_keep, ctypes.c_uint16),
+                                  None if kr is None else _ptr(kr, ctypes.c_uint8),
+                                  None if sr is None else _ptr(sr, ctypes.c_float),
+                                  None if rr is None else _ptr(rr, ctypes.c_uint8), n_rep,
+                                  S, D, flags, _ptr(rows, ctypes.c_int64), n, _ptr(out, ctypes.c_double),
+                                  _ptr(l, ctypes.c_double), _ptr(m, ctypes.c_float))
     return out, l, m
+
+
+def repair_select(v, amax, n_rep: int):
+    """[OVC] "Why V residual repair": the n_rep tokens of largest residual energy (reading R18).
+
+    v: [S, D] bf16 (no V-Smooth: R = V); amax: [D] float32 residual max per channel (all equal for
+    one scale per head). Returns (idx [n_rep] int32 ascending, energy [S] float32, rep [R_pad, D]
+    uint8 E4M3 codes of the kept tokens' rounding residuals in the main codes' units).
+    """
+    v = _u16(v)
+    S, D = v.shape
+    n_rep = int(n_rep)
+    assert 0 <= n_rep <= S
+    a = np.ascontiguousarray(np.broadcast_to(np.asarray(amax, dtype=np.float32), (D,)))
+    idx = np.zeros(max(n_rep, 1), dtype=np.int32)
+    energy = np.empty(max(S, 1), dtype=np.float32)
+    rep = np.zeros((max(nkb_of(n_rep), 1) * BLOCK, D), dtype=np.uint8)
+    lib().orc_repair_select(_ptr(v, ctypes.c_uint16), S, D, _ptr(a, ctypes.c_float), n_rep,
+                            _ptr(idx, ctypes.c_int32), _ptr(energy, ctypes.c_float), _ptr(rep, ctypes.c_uint8))
+    return idx[:n_rep], energy[:S], rep[:nkb_of(n_rep) * BLOCK]
+
+
+def repair_rows(k, v, amax, n_rep: int, kcenter=None) -> dict:
+    """The repair rows of one head: the selected tokens, their keys copied and quantised as extra
+    128-row blocks (minus the K centre when given), and their residual codes."""
+    idx, energy, rep = repair_select(v, amax, n_rep)
+    out = {"n": int(n_rep), "idx": idx, "energy": energy, "rc": rep}
+    if n_rep > 0:
+        out["kc"], out["sk"] = quant_blocks(_u16(k)[idx], center=kcenter)
+    else:
+        out["kc"], out["sk"] = np.zeros((0, _u16(k).shape[1]), dtype=np.uint8), np.zeros(0, dtype=np.float32)
+    return out
 
 
 def attention_exact(q, k, v, rows) -> np.ndarray:
@@ -384,14 +433,16 @@ def attention_demeaned_exact(q, k, v, rows, midwindow: bool = True) -> np.ndarra
 # Whole-path conveniences for one batch-head
 # ----------------------------------------------------------------------------------------------
 def prepare_head(q, k, v, k_clusters: int, iters: int, vsmooth: bool = True, perm=None,
-                 kcenter: bool = False, vscale_channel: bool = False) -> dict:
+                 kcenter: bool = False, vscale_channel: bool = False, n_repair: int = 0) -> dict:
     """Everything the prepare step produces for one batch-head, computed on the CPU.
 
     vsmooth=False: identity permutation, no means (R = V). perm given: use it instead of k-means
     (the parity tests feed the GPU's permutation here, as the acceptance rule says).
     kcenter: subtract the keys' channel mean before their quantisation (see channel_mean_bf16).
     vscale_channel: one residual scale per channel instead of one per head (see demean).
+    n_repair: V residual repair rows (without V-Smooth only; see repair_rows).
     """
+    assert n_repair == 0 or not vsmooth, "V residual repair is defined without V-Smooth"
     q, k, v = _u16(q), _u16(k), _u16(v)
     S, D = q.shape
     out = {"S": S, "D": D}
@@ -414,6 +465,10 @@ def prepare_head(q, k, v, k_clusters: int, iters: int, vsmooth: bool = True, per
                mut=dm.get("mut"))
     out["vsmooth"] = vsmooth
     out["vscale_channel"] = vscale_channel
+    out["repair"] = None
+    if n_repair > 0:
+        amax = dm["amax"] if vscale_channel else np.full(D, dm["amax"], dtype=np.float32)
+        out["repair"] = repair_rows(k, v, amax, n_repair, kcenter=kmu)
     return out
 
 
@@ -421,7 +476,8 @@ def forward_head(prep: dict, rows, expcast: bool = True, midwindow: bool = True)
     flags = (EXPCAST if expcast else 0) | (MIDWINDOW if midwindow else 0)
     mub = prep["mub"] if prep["vsmooth"] else None
     return attention_quant(prep["qc"], prep["sq"], prep["kc"], prep["sk"], prep["rc"], prep["sv"], mub,
-                           prep["S"], rows, flags, mut=prep.get("mut") if prep["vsmooth"] else None)
+                           prep["S"], rows, flags, mut=prep.get("mut") if prep["vsmooth"] else None,
+                           repair=prep.get("repair"))
 
 
 def num_threads() -> int:

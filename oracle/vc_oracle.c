@@ -31,6 +31,12 @@
  *       scale is its residual amax over the whole head / 448 (1 when the channel is all zero), and
  *       the stored block means are bf16(fp32(mean) / scale), so that the single epilogue multiply
  *       by the channel's scale restores both the residual and the mean term.
+ *   R18 V residual repair ([OVC]): the budget is a row count n_rep per head (rho*S rounded up by the
+ *       caller); the energy of a token is summed in fp32 in channel order from its true-unit rounding
+ *       residuals, ties to the lower index; the kept tokens' keys are copied in ascending token order
+ *       into extra 128-row blocks quantised like any other key block (own scale per block); their
+ *       residuals are coded in E4M3 in the main residual codes' units; repair tiles leave the running
+ *       max and the row sum alone (codes clip at 120).  Defined without V-Smooth only.
  */
 #include <math.h>
 #include <stdint.h>
@@ -371,6 +377,70 @@ void orc_demean(const uint16_t* v, const int32_t* perm, int64_t S, int D, int su
   orc_demean_ex(v, perm, S, D, subtract_mean, 0, mu, mub, NULL, resid, rcodes, amax_out, sv_out);
 }
 
+/* ---------------------------------------------------------------------------------------------
+ * V residual repair selection ([OVC] "Why V residual repair"): with the residual quantised without
+ * V-Smooth (R = V, one scale per head or per channel), every token j leaves the rounding residual
+ * r_j,c = s_c (x_j,c - dec(E4M3(x_j,c))), x_j,c = fl32(v_j,c * inv_c); tokens are ranked by the residual
+ * energy sum_c r_j,c^2 and the top n_rep kept.  Reading R18: the energy is taken in fp32 exactly as the
+ * kernel does, t = fl32(s_c * (x - dec)) (the subtraction is exact) and e = fmaf(t, t, e) over
+ * c = 0..D-1 in order; ties go to the lower token index; the kept tokens are listed in ascending
+ * index order.  inv_c = 448/amax_c (1 if amax_c is 0), s_c = amax_c/448 (1 if 0), from the amax of
+ * the residual quantiser (per head: all channels equal).
+ * Outputs: idx [n_rep] ascending, energy [S] (may be NULL), rep [nrt*128, D] E4M3 codes of
+ * (x - dec) for the kept tokens (code units of the main residual codes), pad rows 0. */
+typedef struct {
+  float e;
+  int32_t j;
+} orc_ej;
+
+static int orc_cmp_energy(const void* a, const void* b) {
+  const orc_ej* x = (const orc_ej*)a;
+  const orc_ej* y = (const orc_ej*)b;
+  if (x->e != y->e) return x->e > y->e ? -1 : 1;
+  return x->j < y->j ? -1 : (x->j > y->j);
+}
+
+static int orc_cmp_i32(const void* a, const void* b) {
+  int32_t x = *(const int32_t*)a, y = *(const int32_t*)b;
+  return x < y ? -1 : (x > y);
+}
+
+void orc_repair_select(const uint16_t* v, int64_t S, int D, const float* amax, int64_t n_rep, int32_t* idx,
+                       float* energy, uint8_t* rep) {
+  float* inv = (float*)malloc((size_t)D * sizeof(float));
+  float* sc = (float*)malloc((size_t)D * sizeof(float));
+  for (int d = 0; d < D; ++d) {
+    inv[d] = amax[d] > 0.0f ? 448.0f / amax[d] : 1.0f;
+    sc[d] = amax[d] > 0.0f ? amax[d] / 448.0f : 1.0f;
+  }
+  orc_ej* all = (orc_ej*)malloc((size_t)(S > 0 ? S : 1) * sizeof(orc_ej));
+  for (int64_t j = 0; j < S; ++j) {
+    float e = 0.0f;
+    for (int d = 0; d < D; ++d) {
+      float x = bf16_to_f32(v[j * D + d]) * inv[d];
+      float r = x - (float)orc_e4m3_decode(orc_e4m3_encode(x));
+      float t = sc[d] * r;
+      e = fmaf(t, t, e);
+    }
+    all[j].e = e;
+    all[j].j = (int32_t)j;
+    if (energy) energy[j] = e;
+  }
+  qsort(all, (size_t)S, sizeof(orc_ej), orc_cmp_energy);
+  for (int64_t i = 0; i < n_rep; ++i) idx[i] = all[i].j;
+  qsort(idx, (size_t)n_rep, sizeof(int32_t), orc_cmp_i32);
+  int64_t rpad = (n_rep + ORC_BLOCK - 1) / ORC_BLOCK * ORC_BLOCK;
+  memset(rep, 0, (size_t)(rpad * D));
+  for (int64_t i = 0; i < n_rep; ++i)
+    for (int d = 0; d < D; ++d) {
+      float x = bf16_to_f32(v[(int64_t)idx[i] * D + d]) * inv[d];
+      rep[i * D + d] = orc_e4m3_encode(x - (float)orc_e4m3_decode(orc_e4m3_encode(x)));
+    }
+  free(all);
+  free(inv);
+  free(sc);
+}
+
 /* Gather rows of a [S, D] bf16 tensor by pi: out[t] = x[pi[t]]  ([VC] §3.2 Eq. 3: K' = K[pi]). */
 void orc_gather_rows(const uint16_t* x, const int32_t* perm, int64_t S, int D, uint16_t* out) {
   for (int64_t t = 0; t < S; ++t) memcpy(out + t * D, x + (int64_t)perm[t] * D, (size_t)D * 2);
@@ -412,10 +482,18 @@ float orc_code_scale(int D) { return (float)(8.0 * 1.4426950408889634 / sqrt((do
 
 /* svc: NULL (one residual scale sv per head, means mub in true units) or [D] per-channel scales with mut
  * the means already divided by them (R17): then the mean term is r_j * mut[j,d] and O[d] = svc[d] A[d] / l. */
-void orc_attention_quant_ex(const uint8_t* qc, const float* sq, const uint8_t* kc, const float* sk,
-                            const uint8_t* rc, float sv, const float* svc, const uint16_t* mub, const uint16_t* mut,
-                            int64_t S, int D, int flags, const int64_t* rows, int64_t nrows, double* out,
-                            double* l_out, float* m_out) {
+/* V residual repair ([OVC] "Why V residual repair"), reading R18: n_rep extra key rows visited after
+ * every regular tile, in tiles of 128 (kc_rep [nrt*128, D] codes of the copied keys with one scale per
+ * repair tile sk_rep [nrt]; rc_rep [nrt*128, D] the E4M3 codes of the selected tokens' residuals in the
+ * same code units as rc).  Their probabilities come from the same code formula with the running max M
+ * left as it is (no update, no rescale; ExpCast clips at 120), they add P~ R to the numerator only,
+ * and l is left unchanged.  n_rep = 0: no repair. */
+void orc_attention_quant_rep(const uint8_t* qc, const float* sq, const uint8_t* kc, const float* sk,
+                             const uint8_t* rc, float sv, const float* svc, const uint16_t* mub,
+                             const uint16_t* mut, const uint8_t* kc_rep, const float* sk_rep, const uint8_t* rc_rep,
+                             int64_t n_rep, int64_t S, int D, int flags, const int64_t* rows, int64_t nrows,
+                             double* out, double* l_out, float* m_out) {
+  int nrt = (int)((n_rep + ORC_BLOCK - 1) / ORC_BLOCK);
   int nkb = (int)((S + ORC_BLOCK - 1) / ORC_BLOCK);
   float C = orc_code_scale(D);
 #pragma omp parallel
@@ -479,6 +557,30 @@ void orc_attention_quant_ex(const uint8_t* qc, const float* sq, const uint8_t* k
         }
         l += rj;
       }
+      for (int jr = 0; jr < nrt; ++jr) {  /* repair tiles: numerator only, M kept */
+        int ncols = (int)((int64_t)(jr + 1) * ORC_BLOCK <= n_rep ? ORC_BLOCK : n_rep - (int64_t)jr * ORC_BLOCK);
+        float aj = aq * sk_rep[jr];
+        float b = ORC_B0 - M;
+        for (int c = 0; c < ncols; ++c) {
+          const uint8_t* kr = kc_rep + ((int64_t)jr * ORC_BLOCK + c) * D;
+          double acc = 0.0;
+          for (int d = 0; d < D; ++d) acc += qd[d] * orc_e4m3_decode(kr[d]);
+          float sc = (float)acc;
+          if (flags & ORC_EXPCAST) {
+            code[c] = (uint8_t)orc_expcast_code(sc, aj, b);
+          } else {
+            float y = fmaf(sc, aj, b);
+            float ze = (y - ORC_B0) * 0.125f + 8.0f;
+            code[c] = orc_e4m3_encode((float)exp2((double)ze));
+          }
+        }
+        for (int d = 0; d < D; ++d) {
+          double acc = 0.0;
+          for (int c = 0; c < ncols; ++c)
+            acc += orc_e4m3_decode(code[c]) * orc_e4m3_decode(rc_rep[((int64_t)jr * ORC_BLOCK + c) * D + d]);
+          A[d] += acc;
+        }
+      }
       for (int d = 0; d < D; ++d) out[ri * D + d] = (double)(svc ? svc[d] : sv) * A[d] / l;
       if (l_out) l_out[ri] = l;
       if (m_out) m_out[ri] = M;
@@ -487,6 +589,14 @@ void orc_attention_quant_ex(const uint8_t* qc, const float* sq, const uint8_t* k
     free(A);
     free(qd);
   }
+}
+
+void orc_attention_quant_ex(const uint8_t* qc, const float* sq, const uint8_t* kc, const float* sk,
+                            const uint8_t* rc, float sv, const float* svc, const uint16_t* mub, const uint16_t* mut,
+                            int64_t S, int D, int flags, const int64_t* rows, int64_t nrows, double* out,
+                            double* l_out, float* m_out) {
+  orc_attention_quant_rep(qc, sq, kc, sk, rc, sv, svc, mub, mut, NULL, NULL, NULL, 0, S, D, flags, rows, nrows, out,
+                          l_out, m_out);
 }
 
 void orc_attention_quant(const uint8_t* qc, const float* sq, const uint8_t* kc, const float* sk, const uint8_t* rc,
