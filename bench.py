@@ -319,6 +319,24 @@ def main():
     vc.vc_attn_prepare(Q, K, V, cfg["k"], cfg["iters"], plan=plan)
     torch.cuda.synchronize()
 
+    # V residual repair ("Open-VC Attention", "Why V residual repair"): no V-Smooth, one V scale per
+    # head, the 0.5% of tokens with the largest residual energy repaired; against the same path without.
+    n_rep = vc.repair_rows_for(cfg["S"], 0.005)
+    O_rep = torch.empty_like(O)
+    p_rep = vc.vc_attn_prepare_repair(Q, K, V, n_rep)
+    p_plain = vc.vc_attn_prepare_repair(Q, K, V, 0)
+    rep_flags = vc.VC_EXPCAST | vc.VC_MIDWINDOW
+    repair = {"rho": 0.005, "rows_per_head": n_rep,
+              "prepare_ms": time_it(lambda: vc.vc_attn_prepare_repair(Q, K, V, n_rep, plan=p_rep)),
+              "prepare_ms_no_repair": time_it(lambda: vc.vc_attn_prepare_repair(Q, K, V, 0, plan=p_plain)),
+              "forward_ms": time_it(lambda: vc.vc_attn_forward(p_rep, O_rep, flags=rep_flags)),
+              "forward_ms_no_repair": time_it(lambda: vc.vc_attn_forward(p_plain, O_rep, flags=rep_flags))}
+    repair["forward_overhead_pct"] = 100.0 * (repair["forward_ms"] / repair["forward_ms_no_repair"] - 1.0)
+    p_rep.destroy()
+    p_plain.destroy()
+    del O_rep
+    torch.cuda.synchronize()
+
     # End to end through the public API from pinned host memory, copies inside the timed region.
     e2e = None
     if not args.no_e2e:
@@ -370,6 +388,7 @@ def main():
                                                "group_warm": t_step[vc.VC_STEP_GROUP_WARM],
                                                "reuse": t_step[vc.VC_STEP_REUSE], "plain": t_step[vc.VC_STEP_PLAIN]},
                      "prepare_ms_per_step": sched_prepare_ms},
+        "repair": repair,
         "roofline": {"bound": "tensor", "kernel": "vc_fwd_kernel<128>", "achieved": fwd_tflops, "peak": fp8_peak,
                      "unit": "TFLOP/s", "frac": fwd_tflops / fp8_peak, "traffic": profiled_traffic(cfg),
                      "peak_source": f"{src} bf16 burst {bf16_burst:.0f} TFLOP/s x {FP8_OVER_BF16:.0f} (FP8/BF16 nominal)"},

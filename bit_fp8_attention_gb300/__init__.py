@@ -10,6 +10,7 @@ CPU fallback: if the shared library is missing, calls raise instead of computing
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 
 import torch
@@ -49,11 +50,16 @@ VC_PLAN_CENTROIDS = 10
 VC_PLAN_KCENTER = 11
 VC_PLAN_VCHSCALES = 12
 VC_PLAN_MEANS_T = 13
+VC_PLAN_REPAIR_IDX = 14
+VC_PLAN_REPAIR_ENERGY = 15
+VC_PLAN_REPAIR_KCODES = 16
+VC_PLAN_REPAIR_KSCALES = 17
+VC_PLAN_REPAIR_VCODES = 18
 VC_NOALLOC_MAX_HEADS = 4096
 VC_STEP_GROUP, VC_STEP_GROUP_WARM, VC_STEP_REUSE, VC_STEP_PLAIN = 0, 1, 2, 3
 
-EXPORTS = ("vc_attn_prepare", "vc_attn_prepare_ex", "vc_attn_forward", "vc_plan_size", "vc_plan_get",
-           "vc_plan_status", "vc_plan_shape", "vc_plan_destroy", "vc_expcast_encode", "vc_schedule_action",
+EXPORTS = ("vc_attn_prepare", "vc_attn_prepare_ex", "vc_attn_prepare_repair", "vc_attn_forward", "vc_plan_size",
+           "vc_plan_get", "vc_plan_status", "vc_plan_shape", "vc_plan_destroy", "vc_expcast_encode", "vc_schedule_action",
            "vc_strerror", "vc_version")
 
 
@@ -78,6 +84,7 @@ def lib() -> ctypes.CDLL:
     sigs = {
         "vc_attn_prepare": (i, [vp, vp, vp, i, i, i, i, i, i, vp, ctypes.POINTER(vp)]),
         "vc_attn_prepare_ex": (i, [vp, vp, vp, i, i, i, i, i, i, vp, u, vp, ctypes.POINTER(vp)]),
+        "vc_attn_prepare_repair": (i, [vp, vp, vp, i, i, i, i, i, u, vp, ctypes.POINTER(vp)]),
         "vc_attn_forward": (i, [vp, vp, u, vp]),
         "vc_plan_size": (sz, [vp, i]),
         "vc_plan_get": (i, [vp, i, vp, sz, vp]),
@@ -142,6 +149,9 @@ class Plan:
         self.B, self.H, self.S, self.D, self.k = (d.value for d in dims)
         self.nkb = (self.S + 127) // 128
         self.S_pad = self.nkb * 128
+        # repair rows per head (a plan from vc_attn_prepare_repair); 0 otherwise
+        self.n_repair = lib().vc_plan_size(handle, VC_PLAN_REPAIR_IDX) // (4 * self.B * self.H)
+        self.R_pad = (self.n_repair + 127) // 128 * 128
 
     def destroy(self):
         if self.handle is not None and self.handle.value:
@@ -180,6 +190,20 @@ def vc_attn_prepare_ex(Q, K, V, k_clusters: int, iters: int, perm=None, flags: i
     return plan if plan is not None else Plan(h)
 
 
+def repair_rows_for(S: int, rho: float = 0.005) -> int:
+    """The repair budget as a row count: ceil(rho * S) (the pages' operating point rho = 0.5%)."""
+    return min(S, math.ceil(rho * S))
+
+
+def vc_attn_prepare_repair(Q, K, V, n_repair: int, flags: int = 0, stream=None, plan: Plan | None = None) -> Plan:
+    B, H, S, D = _qkv_args(Q, K, V)
+    h = ctypes.c_void_p(plan.handle.value if plan is not None else None)
+    rc = lib().vc_attn_prepare_repair(Q.data_ptr(), K.data_ptr(), V.data_ptr(), B, H, S, D, n_repair, flags,
+                                      _stream(stream), ctypes.byref(h))
+    _check(rc, "vc_attn_prepare_repair")
+    return plan if plan is not None else Plan(h)
+
+
 def vc_attn_prepare(Q, K, V, k_clusters: int, iters: int, stream=None, plan: Plan | None = None) -> Plan:
     B, H, S, D = _qkv_args(Q, K, V)
     h = ctypes.c_void_p(plan.handle.value if plan is not None else None)
@@ -213,6 +237,11 @@ _PLAN_DTYPES = {
     VC_PLAN_KCENTER: (torch.bfloat16, lambda p: (p.B, p.H, p.D)),
     VC_PLAN_VCHSCALES: (torch.float32, lambda p: (p.B, p.H, p.D)),
     VC_PLAN_MEANS_T: (torch.bfloat16, lambda p: (p.B, p.H, p.D, (p.nkb + 15) // 16 * 16)),
+    VC_PLAN_REPAIR_IDX: (torch.int32, lambda p: (p.B, p.H, p.n_repair)),
+    VC_PLAN_REPAIR_ENERGY: (torch.float32, lambda p: (p.B, p.H, p.S)),
+    VC_PLAN_REPAIR_KCODES: (torch.uint8, lambda p: (p.B, p.H, p.R_pad, p.D)),
+    VC_PLAN_REPAIR_KSCALES: (torch.float32, lambda p: (p.B, p.H, p.R_pad // 128)),
+    VC_PLAN_REPAIR_VCODES: (torch.uint8, lambda p: (p.B, p.H, p.D, p.R_pad)),
 }
 
 

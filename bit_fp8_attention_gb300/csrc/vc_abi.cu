@@ -47,7 +47,7 @@ int check_shape(int B, int H, int S, int D, int k) {
 
 size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
-int plan_create(int B, int H, int S, int D, int k, vc_plan** out) {
+int plan_create(int B, int H, int S, int D, int k, int nrep, vc_plan** out) {
   vc_plan* pl = (vc_plan*)calloc(1, sizeof(vc_plan));
   if (!pl) return VC_ERR_OOM;
   vc::PlanBuffers& b = pl->b;
@@ -57,6 +57,9 @@ int plan_create(int B, int H, int S, int D, int k, vc_plan** out) {
   b.nkb16 = (b.nkb + 15) / 16 * 16;
   b.kpad = (k + 127) / 128 * 128;
   b.nchunk = vc::kmeans_chunks(S);
+  b.nrep = nrep;
+  b.nrt = (nrep + 127) / 128;
+  b.R_pad = b.nrt * 128;
   const size_t BH = (size_t)B * H;
   const size_t codes = BH * b.S_pad * D;
   const size_t sizes[] = {
@@ -83,6 +86,11 @@ int plan_create(int B, int H, int S, int D, int k, vc_plan** out) {
       BH * 4,                         // vamax
       BH * D * 4,                     // vamax_ch
       BH * D * 4,                     // vscales_ch
+      BH * nrep * 4,                  // rep_idx
+      nrep ? BH * S * 4 : 0,          // energy
+      BH * b.R_pad * D,               // krep
+      BH * b.nrt * 4,                 // krep_scales
+      BH * D * b.R_pad,               // vrep
       16,                             // status
   };
   size_t total = 0;
@@ -99,7 +107,9 @@ int plan_create(int B, int H, int S, int D, int k, vc_plan** out) {
                     (void**)&b.perm,   (void**)&b.cent,    (void**)&b.cnorm,   (void**)&b.counts,
                     (void**)&b.offsets, (void**)&b.cent16, (void**)&b.cnormp,  (void**)&b.chist,
                     (void**)&b.kexp,   (void**)&b.ksum,    (void**)&b.kmu,
-                    (void**)&b.vamax,  (void**)&b.vamax_ch, (void**)&b.vscales_ch, (void**)&b.status};
+                    (void**)&b.vamax,  (void**)&b.vamax_ch, (void**)&b.vscales_ch, (void**)&b.rep_idx,
+                    (void**)&b.energy, (void**)&b.krep,     (void**)&b.krep_scales, (void**)&b.vrep,
+                    (void**)&b.status};
   for (size_t i = 0; i < sizeof(sizes) / sizeof(sizes[0]); ++i) {
     *slots[i] = p;
     p += align_up(sizes[i]);
@@ -122,12 +132,8 @@ int plan_create(int B, int H, int S, int D, int k, vc_plan** out) {
   return VC_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-int vc_attn_prepare_ex(const void* Q, const void* K, const void* V, int B, int H, int S, int D, int k_clusters,
-                       int iters, const int32_t* perm, unsigned flags, cudaStream_t stream, vc_plan** plan) {
+int prepare_impl(const void* Q, const void* K, const void* V, int B, int H, int S, int D, int k_clusters, int iters,
+                 const int32_t* perm, unsigned flags, int n_repair, cudaStream_t stream, vc_plan** plan) {
   if (!Q || !K || !V || !plan) return VC_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V)) return VC_ERR_INVALID_ARG;
   int rc = check_shape(B, H, S, D, k_clusters);
@@ -138,6 +144,8 @@ int vc_attn_prepare_ex(const void* Q, const void* K, const void* V, int B, int H
   const bool warm = grouping && (flags & VC_WARM_START) != 0;
   if (grouping && (iters < 1 || iters > kMaxIters)) return VC_ERR_INVALID_ARG;
   if (reuse_perm && perm) return VC_ERR_INVALID_ARG;
+  // Repair rows are defined on the plain per-head (or per-channel) quantisation only.
+  if (n_repair < 0 || n_repair > S || (n_repair > 0 && (vsmooth || reuse_perm))) return VC_ERR_INVALID_ARG;
   // A warm start needs the centroids of an earlier grouping, a reuse the permutation of an earlier
   // prepare: both only on an existing plan.
   if ((warm && !(*plan && (*plan)->b.has_grouping)) || (reuse_perm && !(*plan && (*plan)->b.has_perm)))
@@ -146,9 +154,10 @@ int vc_attn_prepare_ex(const void* Q, const void* K, const void* V, int B, int H
   if (rc != VC_OK) return rc;
   if (*plan) {
     const vc::PlanBuffers& b = (*plan)->b;
-    if (b.B != B || b.H != H || b.S != S || b.D != D || b.k != k_clusters) return VC_ERR_PLAN_MISMATCH;
+    if (b.B != B || b.H != H || b.S != S || b.D != D || b.k != k_clusters || b.nrep != n_repair)
+      return VC_ERR_PLAN_MISMATCH;
   } else {
-    rc = plan_create(B, H, S, D, k_clusters, plan);
+    rc = plan_create(B, H, S, D, k_clusters, n_repair, plan);
     if (rc != VC_OK) return rc;
   }
   vc_plan* pl = *plan;
@@ -163,6 +172,20 @@ int vc_attn_prepare_ex(const void* Q, const void* K, const void* V, int B, int H
     pl->b.has_perm = true;
   }
   return rc;
+}
+
+}  // namespace
+
+extern "C" {
+
+int vc_attn_prepare_ex(const void* Q, const void* K, const void* V, int B, int H, int S, int D, int k_clusters,
+                       int iters, const int32_t* perm, unsigned flags, cudaStream_t stream, vc_plan** plan) {
+  return prepare_impl(Q, K, V, B, H, S, D, k_clusters, iters, perm, flags, 0, stream, plan);
+}
+
+int vc_attn_prepare_repair(const void* Q, const void* K, const void* V, int B, int H, int S, int D, int n_repair,
+                           unsigned flags, cudaStream_t stream, vc_plan** plan) {
+  return prepare_impl(Q, K, V, B, H, S, D, 1, 1, nullptr, flags, n_repair, stream, plan);
 }
 
 int vc_attn_prepare(const void* Q, const void* K, const void* V, int B, int H, int S, int D, int k_clusters,
@@ -195,6 +218,11 @@ size_t vc_plan_size(const vc_plan* plan, int what) {
     case VC_PLAN_KCENTER: return BH * b.D * 2;
     case VC_PLAN_VCHSCALES: return BH * b.D * 4;
     case VC_PLAN_MEANS_T: return BH * b.D * b.nkb16 * 2;
+    case VC_PLAN_REPAIR_IDX: return BH * b.nrep * 4;
+    case VC_PLAN_REPAIR_ENERGY: return b.nrep ? BH * b.S * 4 : 0;
+    case VC_PLAN_REPAIR_KCODES: return BH * b.R_pad * b.D;
+    case VC_PLAN_REPAIR_KSCALES: return BH * b.nrt * 4;
+    case VC_PLAN_REPAIR_VCODES: return BH * b.D * b.R_pad;
     default: return 0;
   }
 }
@@ -218,6 +246,11 @@ int vc_plan_get(const vc_plan* plan, int what, void* dst, size_t bytes, cudaStre
     case VC_PLAN_KCENTER: src = b.kmu; break;
     case VC_PLAN_VCHSCALES: src = b.vscales_ch; break;
     case VC_PLAN_MEANS_T: src = b.meansT; break;
+    case VC_PLAN_REPAIR_IDX: src = b.rep_idx; break;
+    case VC_PLAN_REPAIR_ENERGY: src = b.energy; break;
+    case VC_PLAN_REPAIR_KCODES: src = b.krep; break;
+    case VC_PLAN_REPAIR_KSCALES: src = b.krep_scales; break;
+    case VC_PLAN_REPAIR_VCODES: src = b.vrep; break;
   }
   return cudaMemcpyAsync(dst, src, n, cudaMemcpyDefault, stream) == cudaSuccess ? VC_OK : VC_ERR_CUDA;
 }

@@ -3,6 +3,7 @@
 // Written from the PTX ISA's descriptions of these instructions.
 #pragma once
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -196,6 +197,14 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return (uint32_t)r;
 }
+// E4M3 pair (lo | hi << 8) -> two fp32 values (exact, through f16x2).
+__device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t c) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((uint16_t)c));
+  const __half2 v = *reinterpret_cast<const __half2*>(&h);
+  return __half22float2(v);
+}
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t h16) { return __uint_as_float(h16 << 16); }
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -205,6 +214,27 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// ---- block gather -----------------------------------------------------------------------
+// Gather a block's valid rows (through pi when given) into shared memory, rows >= n zero. Every thread
+// issues all of its loads before it stores any of them.
+template <int D>
+__device__ __forceinline__ void gather_block(uint16_t (*blk)[D], const uint16_t* vh, const int32_t* ph, int t0,
+                                             int n) {
+  constexpr int CPR = D / 8, NCH = 128 * CPR / 256;
+  uint4 w[NCH];
+#pragma unroll
+  for (int m = 0; m < NCH; ++m) {
+    const int c = threadIdx.x + 256 * m, r = c / CPR;
+    w[m] = make_uint4(0, 0, 0, 0);
+    if (r < n) w[m] = __ldg(reinterpret_cast<const uint4*>(vh + (int64_t)(ph ? ph[t0 + r] : t0 + r) * D) + c % CPR);
+  }
+#pragma unroll
+  for (int m = 0; m < NCH; ++m) {
+    const int c = threadIdx.x + 256 * m;
+    *reinterpret_cast<uint4*>(&blk[c / CPR][(c % CPR) * 8]) = w[m];
+  }
 }
 
 }  // namespace vc

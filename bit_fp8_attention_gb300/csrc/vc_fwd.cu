@@ -22,6 +22,9 @@
 //               O/W/l rescale on every increase, E4M3 codes written into TMEM.
 //   warp 8      TMA producer of Q and the K pairs; warp 10 TMA producer of V (with the one-hot rows)
 //               and the mean blocks; warp 9 MMA issuer.
+// V residual repair ("Open-VC Attention", "Why V residual repair"): after every regular tile the CTA
+// visits the plan's repair tiles (copied keys, residual codes) through the same pipeline, with zero
+// one-hot rows (nothing enters W or l) and the running max kept (codes clipped at 120).
 // TMEM columns: O [0, D), W [D, D+16), F [D+16, D+32), l [D+32], P [176, 208) and [208, 240),
 // score buffers S [256, 384) and [384, 512).  P has its own columns so that the commit of S(p+2), which
 // tracks every earlier MMA, also proves that PV(p) has finished reading P(p).
@@ -76,7 +79,9 @@ struct FwdArgs {
   const float* vscales_ch;  // [BH, D] per-channel residual scales, or null (one scale per head)
   uint16_t* out;
   int* status;
+  const float* krep_scales;  // [BH, nrt] scales of the repair key tiles
   int S, S_pad, nkb;
+  int nrt, R_pad;            // repair tiles after the nkb regular ones (0: none), rows per head
   unsigned flags;
   float code_scale;
   int use_mean;
@@ -188,7 +193,7 @@ __device__ __forceinline__ void store_flush_operand(uint32_t tF, const float (&w
   tmem_st16(tF, f);
 }
 
-template <int D, bool kExpCast>
+template <int D, bool kExpCast, bool kRepair>
 __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ FwdMaps maps, const FwdArgs args) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -226,7 +231,10 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qt = blockIdx.x, bh = blockIdx.y;
   const int nkb = args.nkb;
-  const int npairs = (nkb + 1) / 2;
+  // Positions 0..nkb-1 visit the regular key tiles in the chosen order, positions nkb..ntiles-1 the
+  // repair tiles (V residual repair) in order.
+  const int ntiles = kRepair ? nkb + args.nrt : nkb;
+  const int npairs = (ntiles + 1) / 2;
   // Mid-window order shared by the query tiles 2m and 2m+1: start at key tile 2m+2.
   const int start = (args.flags & VC_MIDWINDOW) ? min(nkb - 1, (qt & ~1) + 2) : -1;
   const bool use_mean = args.use_mean != 0;
@@ -259,9 +267,14 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
     if (lane == 0) {
       prefetch_tmap(&maps.q);
       prefetch_tmap(&maps.k);
+      if (kRepair) prefetch_tmap(&maps.krep);
       mbar_arrive_expect_tx(q_full, C::QB);
       tma_load_2d(sQ, &maps.q, 0, bh * args.S_pad + qt * 128, q_full);
-      const int row0 = bh * args.S_pad;
+      const int row0 = bh * args.S_pad, rrow0 = bh * args.R_pad;
+      auto load_k = [&](uint8_t* dst, int t, uint64_t* bar) {
+        if (!kRepair || t < nkb) tma_load_2d(dst, &maps.k, 0, row0 + tile_at(t, start) * 128, bar);
+        else tma_load_2d(dst, &maps.krep, 0, rrow0 + (t - nkb) * 128, bar);
+      };
       int issued_kp = 0;
       bool loads_ok = true;
       for (int k = 0; k < npairs; ++k) {
@@ -269,9 +282,9 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
         const int s = k % C::NKP;
         const int t0 = 2 * k, t1 = 2 * k + 1;
         if (!wait_or_abort(&k_empty[s], ((k / C::NKP) & 1) ^ 1, kWaitLimit, abort_flag)) { loads_ok = false; break; }
-        mbar_arrive_expect_tx(&k_full[s], t1 < nkb ? 2 * C::QB : C::QB);
-        tma_load_2d(sK + s * C::KPB, &maps.k, 0, row0 + tile_at(t0, start) * 128, &k_full[s]);
-        if (t1 < nkb) tma_load_2d(sK + s * C::KPB + C::QB, &maps.k, 0, row0 + tile_at(t1, start) * 128, &k_full[s]);
+        mbar_arrive_expect_tx(&k_full[s], t1 < ntiles ? 2 * C::QB : C::QB);
+        load_k(sK + s * C::KPB, t0, &k_full[s]);
+        if (t1 < ntiles) load_k(sK + s * C::KPB + C::QB, t1, &k_full[s]);
         issued_kp = k + 1;
       }
       if (!loads_ok) record_failure(args.status, abort_flag, kStatusTimeoutLoad);
@@ -292,6 +305,7 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
     if (leader) {
       prefetch_tmap(&maps.v);
       if (use_mean) prefetch_tmap(&maps.mu);
+      if (kRepair) prefetch_tmap(&maps.vrep);
     }
     int issued_v = 0, issued_mu = 0;
     auto leader_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -310,21 +324,23 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
       return true;
     };
     bool loads_ok = true;
-    for (int t = 0; t < nkb && loads_ok; ++t) {
+    for (int t = 0; t < ntiles && loads_ok; ++t) {
       if (warp_aborted(abort_flag)) { loads_ok = false; break; }
-      const int j = tile_at(t, start);
+      const bool regular = !kRepair || t < nkb;
+      const int j = regular ? tile_at(t, start) : t - nkb;
       if (use_mean && t > 0 && seg_start(t, start) && !load_mean_block(tile_at(t - 1, start) >> 4)) {
         loads_ok = false;
         break;
       }
       const int sv = t % C::NV;
       if (t >= C::NV && !leader_wait(&o_done[(t - C::NV) & 3], ((t - C::NV) >> 2) & 1)) { loads_ok = false; break; }
-      {  // one-hot rows: a constant row is invariant under the 16-byte chunk swizzle
+      {  // one-hot rows (all zero under a repair tile: it adds nothing to the row sums); a constant
+         // row is invariant under the 16-byte chunk swizzle
         uint4* onehot = reinterpret_cast<uint4*>(sV + sv * C::VSTAGE + C::VB);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int i = lane + 32 * q;
-          const uint32_t v = ((i >> 3) == (j & 15)) ? 0x38383838u : 0u;
+          const uint32_t v = (regular && (i >> 3) == (j & 15)) ? 0x38383838u : 0u;
           onehot[i] = make_uint4(v, v, v, v);
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -332,7 +348,7 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
       }
       if (leader) {
         mbar_arrive_expect_tx(&v_full[sv], C::VB);
-        tma_load_2d(sV + sv * C::VSTAGE, &maps.v, j * 128, bh * D, &v_full[sv]);
+        tma_load_2d(sV + sv * C::VSTAGE, regular ? &maps.v : &maps.vrep, j * 128, bh * D, &v_full[sv]);
       }
       issued_v = t + 1;
     }
@@ -412,7 +428,7 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
           break;
         }
       }
-      for (int t = 2 * k; t <= 2 * k + 1 && t < nkb; ++t) {
+      for (int t = 2 * k; t <= 2 * k + 1 && t < ntiles; ++t) {
         const int g = t & 1;
         if (!warp_wait(&p_full[g], k & 1, kWaitLimit, abort_flag)) {
           fail(kStatusTimeoutP);
@@ -472,6 +488,7 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
     const uint32_t tS = tmem + lane_base + C::T_S + 128 * wg;
     const uint32_t tP = tmem + lane_base + (wg ? C::T_P1 : C::T_P0);
     const float* skh = args.kscales + (int64_t)bh * nkb;
+    const float* skr = args.krep_scales + (int64_t)bh * args.nrt;
     const float aq = args.code_scale * args.qscales[(int64_t)bh * nkb + qt];
     // One scale per head: the means are in true units and the flush operand carries 1/sV. Per
     // channel: the means are already divided by the channel scales, and the epilogue applies them.
@@ -560,7 +577,7 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
       const float mx = fmaxf(max3f(m8[0], m8[1], m8[2]), max3f(max3f(m8[3], m8[4], m8[5]), m8[6], m8[7]));
       const float aj = aq * sk;
       const float tmax = mx * aj;  // = max_c fl(s_c * a_j): rounding is monotone and a_j > 0
-      if (t + 1 < nkb) {  // the tile max goes to the other group at once; it depends on nothing else
+      if (t + 1 < ntiles) {  // (with repair tiles the last regular tile's max goes over too)  // the tile max goes to the other group at once; it depends on nothing else
         mbuf[(t & 7) * 128 + row] = tmax;
         mbar_arrive(&mx_full[(t & 7) * 4 + wq]);  // release: orders this lane's store before the arrival
       }
@@ -656,9 +673,69 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
       mbar_arrive(&p_full[wg]);
     }
 
+    // Repair tiles (V residual repair): the running max is final after the regular tiles, so there is
+    // no tile max, no rescale and no row-sum flush; the codes are clipped at 120 (a copied key's score
+    // may sit slightly above M) and the zero one-hot rows keep them out of W and l.
+    if constexpr (kRepair) {
+      const int k0 = (nkb - wg + 1) / 2;  // this group's first repair position is 2 k0 + wg
+      if (ok && 2 * k0 + wg - 1 == nkb - 1) {  // the other group had the last regular tile: fold in its max
+        if (!wait_tmax(nkb)) {
+          record_failure(args.status, abort_flag, kStatusTimeoutS);
+          ok = false;
+        } else {
+          Mrun = fmaxf(Mrun, mbuf[((nkb - 1) & 7) * 128 + row]);
+        }
+      }
+      const float bb = __fsub_rn(kB0, Mrun);
+      const uint64_t b2 = pack2f(bb, bb);
+      for (int k = k0; ok; ++k) {
+        const int t = 2 * k + wg;
+        if (t >= ntiles) break;
+        if (warp_aborted(abort_flag)) { ok = false; break; }
+        const float aj = aq * skr[t - nkb];
+        if (!warp_wait(s_full, k & 1, kWaitLimit, abort_flag)) {
+          record_failure(args.status, abort_flag, kStatusTimeoutS);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        known = max(known, 2 * k - 3);
+        uint32_t sr[128];
+        tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
+        tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(s_free);
+        if (!ensure_pv(t - 2)) { ok = false; break; }
+        const uint64_t a2 = pack2f(aj, aj);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int g = 0; g < 16; ++g) {
+            const int c = 64 * h + 4 * g;
+            const float s0 = __uint_as_float(sr[c]), s1 = __uint_as_float(sr[c + 1]);
+            const float s2 = __uint_as_float(sr[c + 2]), s3 = __uint_as_float(sr[c + 3]);
+            if constexpr (kExpCast) {
+              pk[g] = __vminu4(expcast4(s0, s1, s2, s3, a2, a2, b2, b2), 0x78787878u);
+            } else {
+              pk[g] = pack4(expcast_off_code(s0, aj, bb), expcast_off_code(s1, aj, bb), expcast_off_code(s2, aj, bb),
+                            expcast_off_code(s3, aj, bb));
+            }
+          }
+          tmem_st16(tP + 16 * h, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&p_full[wg]);
+      }
+    }
+
     // Group 0 finishes: every PV done, the last run's row sums and means, then O = sV A / l (with
     // per-channel scales O[:, d] = s_d A[:, d] / l).
-    if (wg == 0 && ok && !warp_aborted(abort_flag) && ensure_pv(nkb - 1)) {
+    if (wg == 0 && ok && !warp_aborted(abort_flag) && ensure_pv(ntiles - 1)) {
       float w[16];
       read_w(w);
       float ws = 0.f;
@@ -756,16 +833,21 @@ int encode_fwd_maps(const PlanBuffers& p, FwdMaps* maps) {
   if (rc == VC_OK)
     rc = encode_2d(&maps->mu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.meansT, p.nkb16, BH * p.D, (uint64_t)p.nkb16 * 2,
                    16, p.D, CU_TENSOR_MAP_SWIZZLE_32B);
+  if (rc == VC_OK && p.nrep > 0) {  // repair tiles: the copied keys and the residual codes, same boxes
+    rc = encode_2d(&maps->krep, u8, p.krep, p.D, BH * p.R_pad, p.D, p.D, 128, qsw);
+    if (rc == VC_OK)
+      rc = encode_2d(&maps->vrep, u8, p.vrep, p.R_pad, BH * p.D, p.R_pad, 128, p.D, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
   return rc;
 }
 
-template <int D, bool kExpCast>
+template <int D, bool kExpCast, bool kRepair>
 static int launch_fwd(const PlanBuffers& p, const FwdMaps& maps, uint16_t* O, unsigned flags, cudaStream_t st) {
   using C = FwdCfg<D>;
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(vc_fwd_kernel<D, kExpCast>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(vc_fwd_kernel<D, kExpCast, kRepair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM) != cudaSuccess)
       return VC_ERR_CUDA;
     attr_set = true;
   }
@@ -779,20 +861,30 @@ static int launch_fwd(const PlanBuffers& p, const FwdMaps& maps, uint16_t* O, un
   a.S = p.S;
   a.S_pad = p.S_pad;
   a.nkb = p.nkb;
+  a.nrt = p.nrt;
+  a.R_pad = p.R_pad;
+  a.krep_scales = p.krep_scales;
   a.flags = flags;
   a.code_scale = (float)(8.0 * 1.4426950408889634 / __builtin_sqrt((double)D));
   a.use_mean = (p.has_means && (flags & VC_VSMOOTH)) ? 1 : 0;
+  if (a.use_mean && a.nrt > 0) return VC_ERR_INVALID_ARG;  // repair rows exist only without means
   dim3 grid(p.nkb, p.B * p.H);
-  vc_fwd_kernel<D, kExpCast><<<grid, 352, C::SMEM, st>>>(maps, a);
+  vc_fwd_kernel<D, kExpCast, kRepair><<<grid, 352, C::SMEM, st>>>(maps, a);
   return cudaPeekAtLastError() == cudaSuccess ? VC_OK : VC_ERR_CUDA;
 }
 
+template <int D>
+static int launch_fwd_d(const PlanBuffers& p, const FwdMaps& maps, uint16_t* O, unsigned flags, cudaStream_t st) {
+  const bool ec = (flags & VC_EXPCAST) != 0, rp = p.nrt > 0;
+  if (rp)
+    return ec ? launch_fwd<D, true, true>(p, maps, O, flags, st) : launch_fwd<D, false, true>(p, maps, O, flags, st);
+  return ec ? launch_fwd<D, true, false>(p, maps, O, flags, st) : launch_fwd<D, false, false>(p, maps, O, flags, st);
+}
+
 int forward_launch(const PlanBuffers& p, const FwdMaps& maps, uint16_t* O, unsigned flags, cudaStream_t st) {
-  // ExpCast on and off are separate instantiations, so the default kernel carries only its own code.
-  const bool ec = (flags & VC_EXPCAST) != 0;
-  if (p.D == 128)
-    return ec ? launch_fwd<128, true>(p, maps, O, flags, st) : launch_fwd<128, false>(p, maps, O, flags, st);
-  return ec ? launch_fwd<64, true>(p, maps, O, flags, st) : launch_fwd<64, false>(p, maps, O, flags, st);
+  // ExpCast on/off and repair tiles present/absent are separate instantiations, so the default kernel
+  // carries only its own code.
+  return p.D == 128 ? launch_fwd_d<128>(p, maps, O, flags, st) : launch_fwd_d<64>(p, maps, O, flags, st);
 }
 
 int expcast_launch(const float* s, const float* a, const float* b, int64_t n, uint8_t* out, cudaStream_t st) {

@@ -43,6 +43,13 @@ struct PlanBuffers {
   bool has_vchannel;    // prepared with one residual scale per channel
   int* status;          // [1]
   bool has_means;       // prepared with V-Smooth
+  // V residual repair: n_rep rows per head in nrt = ceil(n_rep/128) extra key tiles (R_pad rows)
+  int nrep, nrt, R_pad;
+  int32_t* rep_idx;     // [BH, nrep] selected tokens, ascending
+  float* energy;        // [BH, S] residual energy of every token
+  uint8_t* krep;        // [BH, R_pad, D] E4M3 codes of the copied keys (pad rows 0)
+  float* krep_scales;   // [BH, nrt]
+  uint8_t* vrep;        // [BH, D, R_pad] E4M3 codes of the selected residuals, transposed (pad 0)
 };
 
 // perm_in: a caller permutation to copy in; reuse_perm: keep the plan's pi (no k-means); otherwise
@@ -59,12 +66,18 @@ int encode_2d(CUtensorMap* m, CUtensorMapDataType dt, void* base, uint64_t inner
               uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw);
 
 struct FwdMaps {
-  CUtensorMap q, k, v, mu;
+  CUtensorMap q, k, v, mu, krep, vrep;
 };
 int encode_fwd_maps(const PlanBuffers& p, FwdMaps* maps);
 int forward_launch(const PlanBuffers& p, const FwdMaps& maps, uint16_t* O, unsigned flags, cudaStream_t st);
 int residual_pack_launch(const uint16_t* V, const int32_t* perm, int BH, int S, int D, uint16_t* means,
                          uint8_t* vcodes, float* vscales, unsigned int* amax_scratch, cudaStream_t st);
+// Block quantiser: S rows per head (through perm [BH, S] when given) of a source with S_src rows per head.
+void quant_blocks_launch(const uint16_t* x, const int32_t* perm, const uint16_t* center, int D, int S, int S_pad,
+                         int S_src, int BH, uint8_t* codes, float* scales, cudaStream_t st);
+// V residual repair rows (no V-Smooth): energies, selection, copied keys, residual codes. kcen: the K
+// centre or null. The residual maxima (vamax, or vamax_ch when has_vchannel) must be complete.
+int repair_launch(const PlanBuffers& p, const uint16_t* K, const uint16_t* V, const uint16_t* kcen, cudaStream_t st);
 int expcast_launch(const float* s, const float* a, const float* b, int64_t n, uint8_t* out, cudaStream_t st);
 
 }  // namespace vc

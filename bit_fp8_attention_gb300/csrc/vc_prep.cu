@@ -16,7 +16,6 @@
 
 namespace vc {
 
-static __device__ __forceinline__ float bf16_bits_to_f32(uint32_t h16) { return __uint_as_float(h16 << 16); }
 
 // Round a double to bf16, to nearest even, in one step (no intermediate fp32 rounding).
 static __device__ uint16_t f64_to_bf16_rne(double x) {
@@ -49,47 +48,57 @@ static __device__ uint16_t f64_to_bf16_rne(double x) {
 // when it is given (the K' = K[pi] gather), otherwise in order.  amax over the whole 128 x D
 // block, scale = amax/448, code = E4M3_rne_satfinite(x * (448/amax)); pad rows get code 0.
 // ---------------------------------------------------------------------------------------------
-// One element of a 16-byte chunk of 8 bf16, as fp32, minus the matching centre element if any.
-__device__ __forceinline__ float chunk_elem(const uint4& w, const uint4& c, bool centred, int i) {
+// One element of a 16-byte chunk of 8 bf16, as fp32, minus the matching centre element when centred.
+template <bool kCentred>
+__device__ __forceinline__ float chunk_elem(const uint4& w, const uint4& c, int i) {
   const uint32_t* wv = reinterpret_cast<const uint32_t*>(&w);
   const uint32_t* cv = reinterpret_cast<const uint32_t*>(&c);
   const int sh = (i & 1) * 16;
   float f = bf16_bits_to_f32((wv[i >> 1] >> sh) & 0xFFFFu);
-  if (centred) f = __fsub_rn(f, bf16_bits_to_f32((cv[i >> 1] >> sh) & 0xFFFFu));
+  if (kCentred) f = __fsub_rn(f, bf16_bits_to_f32((cv[i >> 1] >> sh) & 0xFFFFu));
   return f;
 }
 
 // Per-128-token block E4M3 quantisation of Q (token order) or K (gathered through pi, optionally minus
 // the head's channel centre): one CTA per (block, bh), amax over the valid rows, scale = amax/448,
-// code = E4M3_RNE_sat(x * (448/amax)); pad rows are code 0.
-template <int D>
+// code = E4M3_RNE_sat(x * (448/amax)); pad rows are code 0.  Every thread issues all of its row loads
+// before it uses any of them.  S rows per head are coded (perm: [BH, S] source rows); the source
+// tensor holds S_src rows per head.
+template <int D, bool kCentred>
 __global__ void __launch_bounds__(256) quant_blocks_kernel(const uint16_t* __restrict__ x,
                                                            const int32_t* __restrict__ perm,
                                                            const uint16_t* __restrict__ center, int S, int S_pad,
-                                                           uint8_t* __restrict__ codes, float* __restrict__ scales) {
+                                                           int S_src, uint8_t* __restrict__ codes,
+                                                           float* __restrict__ scales) {
   constexpr int CPR = D / 8;                 // 16-byte chunks per row
   constexpr int NCH = 128 * CPR / 256;       // chunks per thread
   const int j = blockIdx.x, bh = blockIdx.y;
   const int nkb = S_pad / 128;
-  const uint16_t* xh = x + (int64_t)bh * S * D;
+  const uint16_t* xh = x + (int64_t)bh * S_src * D;
   const int32_t* ph = perm ? perm + (int64_t)bh * S : nullptr;
-  const bool centred = center != nullptr;
-  uint4 v[NCH], cen[NCH];
+  __shared__ uint4 cen_s[CPR];
+  __shared__ float red[8];
+  if (kCentred && threadIdx.x < CPR)
+    cen_s[threadIdx.x] = __ldg(reinterpret_cast<const uint4*>(center + (int64_t)bh * D) + threadIdx.x);
+  uint4 v[NCH];
+#pragma unroll
+  for (int m = 0; m < NCH; ++m) {
+    const int c = threadIdx.x + 256 * m;
+    const int t = j * 128 + c / CPR;
+    v[m] = make_uint4(0, 0, 0, 0);
+    if (t < S) v[m] = *reinterpret_cast<const uint4*>(xh + (int64_t)(ph ? ph[t] : t) * D + (c % CPR) * 8);
+  }
+  if (kCentred) __syncthreads();
   float amax = 0.f;
 #pragma unroll
   for (int m = 0; m < NCH; ++m) {
-    int c = threadIdx.x + 256 * m;
-    int r = c / CPR, cc = c % CPR;
-    int t = j * 128 + r;
-    cen[m] = centred ? __ldg(reinterpret_cast<const uint4*>(center + (int64_t)bh * D) + cc) : make_uint4(0, 0, 0, 0);
-    if (t < S) {
-      int src = ph ? ph[t] : t;
-      v[m] = *reinterpret_cast<const uint4*>(xh + (int64_t)src * D + cc * 8);
+    const int c = threadIdx.x + 256 * m;
+    const uint4 cm = kCentred ? cen_s[c % CPR] : make_uint4(0, 0, 0, 0);
+    float a = 0.f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(chunk_elem(v[m], cen[m], centred, i)));
-    }
+    for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(chunk_elem<kCentred>(v[m], cm, i)));
+    if (j * 128 + c / CPR < S) amax = fmaxf(amax, a);  // pad rows do not count
   }
-  __shared__ float red[8];
 #pragma unroll
   for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
@@ -103,19 +112,33 @@ __global__ void __launch_bounds__(256) quant_blocks_kernel(const uint16_t* __res
   uint8_t* ch = codes + ((int64_t)bh * S_pad + (int64_t)j * 128) * D;
 #pragma unroll
   for (int m = 0; m < NCH; ++m) {
-    int c = threadIdx.x + 256 * m;
-    int r = c / CPR, cc = c % CPR;
+    const int c = threadIdx.x + 256 * m;
+    const int r = c / CPR, cc = c % CPR;
+    const uint4 cm = kCentred ? cen_s[cc] : make_uint4(0, 0, 0, 0);
     uint32_t lo = 0, hi = 0;
     if (!zero && j * 128 + r < S) {
       uint32_t w[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        w[q] = cvt_e4m3x2(__fmul_rn(chunk_elem(v[m], cen[m], centred, 2 * q), inv),
-                          __fmul_rn(chunk_elem(v[m], cen[m], centred, 2 * q + 1), inv));
+        w[q] = cvt_e4m3x2(__fmul_rn(chunk_elem<kCentred>(v[m], cm, 2 * q), inv),
+                          __fmul_rn(chunk_elem<kCentred>(v[m], cm, 2 * q + 1), inv));
       lo = w[0] | (w[1] << 16);
       hi = w[2] | (w[3] << 16);
     }
     *reinterpret_cast<uint2*>(ch + (int64_t)r * D + cc * 8) = make_uint2(lo, hi);
+  }
+}
+
+// Launch of the block quantiser for D in {64, 128}, centred or not (grid: S_pad/128 x BH).
+void quant_blocks_launch(const uint16_t* x, const int32_t* perm, const uint16_t* center, int D, int S, int S_pad,
+                         int S_src, int BH, uint8_t* codes, float* scales, cudaStream_t st) {
+  const dim3 grid(S_pad / 128, BH);
+  if (D == 128) {
+    if (center) quant_blocks_kernel<128, true><<<grid, 256, 0, st>>>(x, perm, center, S, S_pad, S_src, codes, scales);
+    else quant_blocks_kernel<128, false><<<grid, 256, 0, st>>>(x, perm, nullptr, S, S_pad, S_src, codes, scales);
+  } else {
+    if (center) quant_blocks_kernel<64, true><<<grid, 256, 0, st>>>(x, perm, center, S, S_pad, S_src, codes, scales);
+    else quant_blocks_kernel<64, false><<<grid, 256, 0, st>>>(x, perm, nullptr, S, S_pad, S_src, codes, scales);
   }
 }
 
@@ -216,12 +239,7 @@ __global__ void __launch_bounds__(256) vmeans_kernel(const uint16_t* __restrict_
   __shared__ float mus[D];
   __shared__ float red[8];
   __shared__ float cmax[SPLIT][D];
-  constexpr int CPR = D / 8;  // 16-byte chunks per row
-  for (int c = threadIdx.x; c < n * CPR; c += 256) {
-    const int r = c / CPR, cc = c % CPR;
-    const int src = ph ? ph[t0 + r] : t0 + r;
-    *reinterpret_cast<uint4*>(&blk[r][cc * 8]) = __ldg(reinterpret_cast<const uint4*>(vh + (int64_t)src * D) + cc);
-  }
+  gather_block<D>(blk, vh, ph, t0, n);
   __syncthreads();
   // exponent field with subnormals and zero read as 1, as in M * 2^(E - 134)
   int em = 1;
@@ -320,12 +338,7 @@ __global__ void __launch_bounds__(256) vpack_kernel(const uint16_t* __restrict__
       if (j == 0 && svc) svc[(int64_t)bh * D + d] = sv_h;
     }
   }
-  constexpr int CPR = D / 8;  // 16-byte chunks per row
-  for (int c = threadIdx.x; c < n * CPR; c += 256) {
-    const int r = c / CPR, cc = c % CPR;
-    const int src = ph ? ph[t0 + r] : t0 + r;
-    *reinterpret_cast<uint4*>(&blk[r][cc * 8]) = __ldg(reinterpret_cast<const uint4*>(vh + (int64_t)src * D) + cc);
-  }
+  gather_block<D>(blk, vh, ph, t0, n);
   __syncthreads();
   uint8_t* out = vt + (int64_t)bh * D * S_pad + (int64_t)t0;
   for (int task = threadIdx.x; task < D * 4; task += 256) {
@@ -361,8 +374,7 @@ int prepare_launch(const PlanBuffers& p, const uint16_t* Q, const uint16_t* K, c
   const int BH = p.B * p.H, S = p.S, D = p.D, nkb = p.nkb, S_pad = p.S_pad;
   dim3 gblk(nkb, BH);
   // Q: per-block quantisation in token order
-  if (D == 128) quant_blocks_kernel<128><<<gblk, 256, 0, st>>>(Q, nullptr, nullptr, S, S_pad, p.qcodes, p.qscales);
-  else quant_blocks_kernel<64><<<gblk, 256, 0, st>>>(Q, nullptr, nullptr, S, S_pad, p.qcodes, p.qscales);
+  quant_blocks_launch(Q, nullptr, nullptr, D, S, S_pad, S, BH, p.qcodes, p.qscales, st);
   if (check_launch()) return VC_ERR_CUDA;
   const int32_t* perm = nullptr;
   if (reuse_perm) {  // the permutation of an earlier prepare stays (grouping schedule)
@@ -398,8 +410,7 @@ int prepare_launch(const PlanBuffers& p, const uint16_t* Q, const uint16_t* K, c
     kstat_mean_kernel<<<(BH * D + 255) / 256, 256, 0, st>>>(p.kexp, p.ksum, S, BH * D, p.kmu);
     kcen = p.kmu;
   }
-  if (D == 128) quant_blocks_kernel<128><<<gblk, 256, 0, st>>>(K, perm, kcen, S, S_pad, p.kcodes, p.kscales);
-  else quant_blocks_kernel<64><<<gblk, 256, 0, st>>>(K, perm, kcen, S, S_pad, p.kcodes, p.kscales);
+  quant_blocks_launch(K, perm, kcen, D, S, S_pad, S, BH, p.kcodes, p.kscales, st);
   // V' = V[pi]: block means, residual maximum per head, residual codes transposed
   if (cudaMemsetAsync(p.vamax, 0, sizeof(unsigned int) * BH, st) != cudaSuccess) return VC_ERR_CUDA;
   unsigned int* ach = vchannel ? p.vamax_ch : nullptr;
@@ -414,7 +425,8 @@ int prepare_launch(const PlanBuffers& p, const uint16_t* Q, const uint16_t* K, c
     vpack_kernel<64><<<gblk, 256, 0, st>>>(V, perm, S, S_pad, p.means, p.vamax, p.vcodes, p.vscales, ach,
                                            p.vscales_ch, p.meansT, p.nkb16);
   }
-  return check_launch();
+  if (check_launch()) return VC_ERR_CUDA;
+  return repair_launch(p, K, V, kcen, st);  // nothing without repair rows
 }
 
 }  // namespace vc

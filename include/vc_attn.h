@@ -124,6 +124,25 @@ int vc_attn_prepare(const void* Q, const void* K, const void* V, int B, int H, i
 int vc_attn_prepare_ex(const void* Q, const void* K, const void* V, int B, int H, int S, int D, int k_clusters,
                        int iters, const int32_t* perm, unsigned flags, cudaStream_t stream, vc_plan** plan);
 
+/* vc_attn_prepare_repair -- prepare without V-Smooth, plus V residual repair rows ("Open-VC
+ * Attention", "Why V residual repair").
+ * Per (b, h): Q and K quantised per 128-token block, V quantised per head (or per channel with
+ * VC_VSCALE_CHANNEL) as in vc_attn_prepare_ex without VC_VSMOOTH; then every token j gets the energy
+ *   e_j = sum_c (s_c * (x_jc - E4M3(x_jc)))^2,  x_jc = fl32(V_jc * 448 / amax_c),
+ * accumulated as fp32 fused multiply-adds in channel order; the n_repair tokens of largest energy
+ * (ties to the lower index) are kept in ascending token order. Their bf16 keys are copied into
+ * ceil(n_repair/128) extra key blocks, quantised like any key block (one scale per block, minus the
+ * K centre with VC_KCENTER), and their residuals x - E4M3(x) are coded in E4M3 in the same code units
+ * as the main residual codes. The forward visits these repair tiles after every regular tile; they
+ * neither raise the running max (their codes clip at 120) nor add to the row sum, so they change the
+ * numerator only.
+ * n_repair: 0 <= n_repair <= S rows per head (the pages' operating point is ceil(0.005 * S)); it is
+ *   part of the plan's shape (VC_ERR_PLAN_MISMATCH when an existing plan has another count).
+ * flags: VC_KCENTER | VC_VSCALE_CHANNEL; VC_VSMOOTH or VC_REUSE_PERM -> VC_ERR_INVALID_ARG.
+ * Other arguments, allocation and asynchrony as vc_attn_prepare. */
+int vc_attn_prepare_repair(const void* Q, const void* K, const void* V, int B, int H, int S, int D, int n_repair,
+                           unsigned flags, cudaStream_t stream, vc_plan** plan);
+
 /* vc_attn_forward
  * The fused attention forward (VC-Attention Eq. 1, 6, 7): for every query row, key tiles of
  * 128 are visited in the chosen order; S = Q K'^T on FP8 tensor cores; the running maximum is
@@ -155,10 +174,17 @@ enum {
   VC_PLAN_KCENTER = 11,  /* bf16  [B, H, D]        K channel centre (prepared with VC_KCENTER) */
   VC_PLAN_VCHSCALES = 12, /* fp32 [B, H, D]        the residual scale of each channel (all equal
                                                      to the head's scale without VC_VSCALE_CHANNEL) */
-  VC_PLAN_MEANS_T = 13   /* bf16  [B, H, D, nkb16] the means as the forward reads them: transposed,
+  VC_PLAN_MEANS_T = 13,  /* bf16  [B, H, D, nkb16] the means as the forward reads them: transposed,
                                                      nkb16 = 16*ceil(nkb/16) with zero pad columns,
                                                      divided by the channel scale with
                                                      VC_VSCALE_CHANNEL, else in true units         */
+  VC_PLAN_REPAIR_IDX = 14,     /* int32 [B, H, n_repair]  repaired tokens, ascending                */
+  VC_PLAN_REPAIR_ENERGY = 15,  /* fp32  [B, H, S]         residual energy of every token            */
+  VC_PLAN_REPAIR_KCODES = 16,  /* uint8 [B, H, R_pad, D]  E4M3 codes of the copied keys (pad rows 0),
+                                                          R_pad = 128 * ceil(n_repair / 128)        */
+  VC_PLAN_REPAIR_KSCALES = 17, /* fp32  [B, H, R_pad/128] one scale per repair key block           */
+  VC_PLAN_REPAIR_VCODES = 18   /* uint8 [B, H, D, R_pad]  E4M3 codes of the repaired residuals,
+                                                          transposed (pad 0)                        */
 };
 /* Size in bytes of one plan tensor (0 for an unknown `what` or a NULL plan). */
 size_t vc_plan_size(const vc_plan* plan, int what);

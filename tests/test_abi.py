@@ -86,6 +86,12 @@ def test_invalid_arguments_rejected_without_device(L):
     assert L.vc_attn_prepare_ex(fake, fake, fake, 1, 1, 128, 128, 1, 2, None, 2 | 16, None, ctypes.byref(plan)) == -1
     assert L.vc_attn_prepare_ex(fake, fake, fake, 1, 1, 128, 128, 1, 2, None, 2 | 32, None, ctypes.byref(plan)) == -1
     assert L.vc_attn_prepare_ex(fake, fake, fake, 1, 1, 128, 128, 1, 2, fake, 2 | 32, None, ctypes.byref(plan)) == -1
+    # repair rows: count within [0, S], never with V-Smooth or a reused permutation
+    assert L.vc_attn_prepare_repair(fake, fake, fake, 1, 1, 128, 128, -1, 0, None, ctypes.byref(plan)) == -1
+    assert L.vc_attn_prepare_repair(fake, fake, fake, 1, 1, 128, 128, 129, 0, None, ctypes.byref(plan)) == -1
+    assert L.vc_attn_prepare_repair(fake, fake, fake, 1, 1, 128, 128, 4, 2, None, ctypes.byref(plan)) == -1
+    assert L.vc_attn_prepare_repair(fake, fake, fake, 1, 1, 128, 128, 4, 32, None, ctypes.byref(plan)) == -1
+    assert L.vc_attn_prepare_repair(None, fake, fake, 1, 1, 128, 128, 4, 0, None, ctypes.byref(plan)) == -1
     assert plan.value is None
     # forward / plan calls on a null plan
     assert L.vc_attn_forward(None, fake, 7, None) == -1
