@@ -61,13 +61,18 @@ def workload_name(cfg):
             f"grid={'x'.join(map(str, cfg['grid']))} k={cfg['k']} iters={cfg['iters']}")
 
 
-FWD_SOURCES = ("vc_fwd.cu", "vc_device.cuh", "vc_internal.h")
+FWD_SOURCES = ("vc_fwd.cu", "vc_fwd_common.cuh", "vc_device.cuh", "vc_internal.h")  # the D = 128 kernel
+FWD2_SOURCES = ("vc_fwd2.cu", "vc_fwd_common.cuh", "vc_device.cuh", "vc_internal.h")  # the D = 64 kernel
 
 
-def forward_source_hash() -> str:
+def forward_kernel_name(D: int) -> str:
+    return "vc_fwd_kernel<128>" if D == 128 else "vc_fwd2_kernel<64>"
+
+
+def forward_source_hash(D: int = 128) -> str:
     """First 16 hex digits of the sha256 of the forward kernel's sources (which ncu counters are valid for)."""
     h = hashlib.sha256()
-    for name in FWD_SOURCES:
+    for name in (FWD_SOURCES if D == 128 else FWD2_SOURCES):
         with open(os.path.join(ROOT, "bit_fp8_attention_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -84,7 +89,7 @@ def profiled_traffic(cfg):
         return None
     m_hash = re.search(r"forward source sha256/16: `?([0-9a-f]{16})", text)
     m_bytes = re.search(r"traffic per launch: (\d+) bytes", text)
-    if not (m_hash and m_bytes) or m_hash.group(1) != forward_source_hash():
+    if not (m_hash and m_bytes) or m_hash.group(1) != forward_source_hash(cfg["D"]):
         return None
     return int(m_bytes.group(1))
 
@@ -389,7 +394,8 @@ def main():
                                                "reuse": t_step[vc.VC_STEP_REUSE], "plain": t_step[vc.VC_STEP_PLAIN]},
                      "prepare_ms_per_step": sched_prepare_ms},
         "repair": repair,
-        "roofline": {"bound": "tensor", "kernel": "vc_fwd_kernel<128>", "achieved": fwd_tflops, "peak": fp8_peak,
+        "roofline": {"bound": "tensor", "kernel": forward_kernel_name(cfg["D"]), "achieved": fwd_tflops,
+                     "peak": fp8_peak,
                      "unit": "TFLOP/s", "frac": fwd_tflops / fp8_peak, "traffic": profiled_traffic(cfg),
                      "peak_source": f"{src} bf16 burst {bf16_burst:.0f} TFLOP/s x {FP8_OVER_BF16:.0f} (FP8/BF16 nominal)"},
         "clocks": clocks, "gpu_launches": launches_per_step(cfg) * args.steps,

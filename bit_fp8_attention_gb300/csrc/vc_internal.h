@@ -70,6 +70,7 @@ struct FwdMaps {
 };
 int encode_fwd_maps(const PlanBuffers& p, FwdMaps* maps);
 int forward_launch(const PlanBuffers& p, const FwdMaps& maps, uint16_t* O, unsigned flags, cudaStream_t st);
+int forward2_launch(const PlanBuffers& p, const FwdMaps& maps, uint16_t* O, unsigned flags, cudaStream_t st);
 int residual_pack_launch(const uint16_t* V, const int32_t* perm, int BH, int S, int D, uint16_t* means,
                          uint8_t* vcodes, float* vscales, unsigned int* amax_scratch, cudaStream_t st);
 // Block quantiser: S rows per head (through perm [BH, S] when given) of a source with S_src rows per head.
