@@ -7,7 +7,8 @@
 // score with every increase applied, row sum of the decoded FP8 probabilities that feed PV,
 // mid-window key order, packed transposed V.
 //
-// GB300 design (not the pages' kernel): one CTA per 128-row query tile and batch-head.
+// GB300 design (not the pages' kernel): one CTA per 128-row query tile and batch-head. This kernel serves
+// D = 128; D = 64 runs the two-query-tile kernel of vc_fwd2.cu.
 //   producer    TMA: Q once; K' and V^T tiles of 128 keys into 3-stage rings; with
 //               V-Smooth, the transposed bf16 means of each 16-tile block run into a 2-stage ring.
 //   MMA issuer  one warp, one elected lane issuing: S = Q K'^T for two key tiles at once
@@ -777,12 +778,12 @@ static int launch_fwd_d(const PlanBuffers& p, const FwdMaps& maps, uint16_t* O, 
 }
 
 int forward_launch(const PlanBuffers& p, const FwdMaps& maps, uint16_t* O, unsigned flags, cudaStream_t st) {
-  // D = 64 without repair tiles: the two-query-tile kernel (vc_fwd2.cu), faster there; at D = 128 its
-  // score buffers must be split into halves to fit TMEM, and the one-query-tile kernel is faster.
-  if (p.D == 64 && p.nrt == 0) return forward2_launch(p, maps, O, flags, st);
+  // D = 64: the two-query-tile kernel (vc_fwd2.cu), faster there; at D = 128 its score buffers must be
+  // split into halves to fit TMEM, and the one-query-tile kernel is faster.
+  if (p.D == 64) return forward2_launch(p, maps, O, flags, st);
   // ExpCast on/off and repair tiles present/absent are separate instantiations, so the default kernel
   // carries only its own code.
-  return p.D == 128 ? launch_fwd_d<128>(p, maps, O, flags, st) : launch_fwd_d<64>(p, maps, O, flags, st);
+  return launch_fwd_d<128>(p, maps, O, flags, st);
 }
 
 int expcast_launch(const float* s, const float* a, const float* b, int64_t n, uint8_t* out, cudaStream_t st) {

@@ -54,7 +54,7 @@ struct Fwd2Cfg {
   static_assert(T_F + 16 <= T_S, "TMEM columns of one group");
 };
 
-template <int D, bool kExpCast>
+template <int D, bool kExpCast, bool kRepair>
 __global__ void __launch_bounds__(352, 1) vc_fwd2_kernel(const __grid_constant__ FwdMaps maps, const FwdArgs args) {
   using C = Fwd2Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -88,6 +88,8 @@ __global__ void __launch_bounds__(352, 1) vc_fwd2_kernel(const __grid_constant__
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int pair = blockIdx.x, bh = blockIdx.y;
   const int nkb = args.nkb;
+  // Positions 0..nkb-1 visit the regular key tiles in the chosen order, nkb..ntiles-1 the repair tiles.
+  const int ntiles = kRepair ? nkb + args.nrt : nkb;
   const int q0 = 2 * pair;  // query tiles q0 (group 0) and q0 + 1 (group 1; past the end when nkb is odd)
   const int start = (args.flags & VC_MIDWINDOW) ? min(nkb - 1, q0 + 2) : -1;
   const bool use_mean = args.use_mean != 0;
@@ -119,6 +121,7 @@ __global__ void __launch_bounds__(352, 1) vc_fwd2_kernel(const __grid_constant__
     if (lane == 0) {
       prefetch_tmap(&maps.q);
       prefetch_tmap(&maps.k);
+      if (kRepair) prefetch_tmap(&maps.krep);
       const int row0 = bh * args.S_pad;
       // The second Q tile of the last pair of an odd nkb starts past this head: the next head's
       // rows, or past the tensor (zero fill); its rows are never stored.
@@ -127,12 +130,13 @@ __global__ void __launch_bounds__(352, 1) vc_fwd2_kernel(const __grid_constant__
       tma_load_2d(sQ + C::QB, &maps.q, 0, row0 + (q0 + 1) * 128, q_full);
       int issued = 0;
       bool loads_ok = true;
-      for (int t = 0; t < nkb; ++t) {
+      for (int t = 0; t < ntiles; ++t) {
         if (*abort_flag) { loads_ok = false; break; }
         const int s = t % C::NK;
         if (!wait_or_abort(&k_empty[s], ((t / C::NK) & 1) ^ 1, kWaitLimit, abort_flag)) { loads_ok = false; break; }
         mbar_arrive_expect_tx(&k_full[s], C::QB);
-        tma_load_2d(sK + s * C::QB, &maps.k, 0, row0 + tile_at(t, start) * 128, &k_full[s]);
+        if (!kRepair || t < nkb) tma_load_2d(sK + s * C::QB, &maps.k, 0, row0 + tile_at(t, start) * 128, &k_full[s]);
+        else tma_load_2d(sK + s * C::QB, &maps.krep, 0, bh * args.R_pad + (t - nkb) * 128, &k_full[s]);
         issued = t + 1;
       }
       if (!loads_ok) record_failure(args.status, abort_flag, kStatusTimeoutLoad);
@@ -150,6 +154,7 @@ __global__ void __launch_bounds__(352, 1) vc_fwd2_kernel(const __grid_constant__
     if (leader) {
       prefetch_tmap(&maps.v);
       if (use_mean) prefetch_tmap(&maps.mu);
+      if (kRepair) prefetch_tmap(&maps.vrep);
     }
     int issued_v = 0, issued_mu = 0;
     auto leader_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -168,9 +173,10 @@ __global__ void __launch_bounds__(352, 1) vc_fwd2_kernel(const __grid_constant__
       return true;
     };
     bool loads_ok = true;
-    for (int t = 0; t < nkb && loads_ok; ++t) {
+    for (int t = 0; t < ntiles && loads_ok; ++t) {
       if (warp_aborted(abort_flag)) { loads_ok = false; break; }
-      const int j = tile_at(t, start);
+      const bool regular = !kRepair || t < nkb;  // a repair tile has zero one-hot rows: nothing enters W
+      const int j = regular ? tile_at(t, start) : t - nkb;
       if (use_mean && t > 0 && seg_start(t, start) && !load_mean_block(tile_at(t - 1, start) >> 4)) {
         loads_ok = false;
         break;
@@ -182,7 +188,7 @@ __global__ void __launch_bounds__(352, 1) vc_fwd2_kernel(const __grid_constant__
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int i = lane + 32 * q;
-          const uint32_t v = ((i >> 3) == (j & 15)) ? 0x38383838u : 0u;
+          const uint32_t v = (regular && (i >> 3) == (j & 15)) ? 0x38383838u : 0u;
           onehot[i] = make_uint4(v, v, v, v);
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -190,7 +196,7 @@ __global__ void __launch_bounds__(352, 1) vc_fwd2_kernel(const __grid_constant__
       }
       if (leader) {
         mbar_arrive_expect_tx(&v_full[sv], C::VB);
-        tma_load_2d(sV + sv * C::VSTAGE, &maps.v, j * 128, bh * D, &v_full[sv]);
+        tma_load_2d(sV + sv * C::VSTAGE, regular ? &maps.v : &maps.vrep, j * 128, bh * D, &v_full[sv]);
       }
       issued_v = t + 1;
     }
@@ -260,14 +266,14 @@ __global__ void __launch_bounds__(352, 1) vc_fwd2_kernel(const __grid_constant__
               issue_qk(0, 0, 0) && issue_qk(1, 0, 0);
     if (!ok) fail(kStatusTimeoutLoad);
     int seg = -1;  // ordinal of the current block run
-    for (int t = 0; ok && t < nkb; ++t) {
+    for (int t = 0; ok && t < ntiles; ++t) {
       for (int h = 1; ok && h < C::NH; ++h) {
         if (!issue_qk(0, t, h) || !issue_qk(1, t, h)) { fail(kStatusTimeoutP); ok = false; }
       }
       if (!ok) break;
       if (leader) mma_commit(&k_empty[t % C::NK]);  // every score MMA of tile t is issued
       __syncwarp();
-      if (t + 1 < nkb) {
+      if (t + 1 < ntiles) {
         if (!warp_wait(&k_full[(t + 1) % C::NK], ((t + 1) / C::NK) & 1, kWaitLimit, abort_flag)) {
           fail(kStatusTimeoutLoad);
           break;
@@ -353,21 +359,16 @@ __global__ void __launch_bounds__(352, 1) vc_fwd2_kernel(const __grid_constant__
 #pragma unroll
       for (int s = 0; s < 16; ++s) w[s] = __uint_as_float(wr[s]);
     };
-    float sk_next = skh[tile_at(0, start)];
-    for (int t = 0; ok && t < nkb; ++t) {
-      if (warp_aborted(abort_flag)) { ok = false; break; }
-      const int j = tile_at(t, start);
-      const float sk = sk_next;
-      if (t + 1 < nkb) sk_next = skh[tile_at(t + 1, start)];
-      float s[128];
+    // The 128 raw scores of position t, sub-tile by sub-tile; each sub-tile's buffer is released as soon
+    // as it is in registers.
+    auto load_scores = [&](int t, float(&s)[128]) -> bool {
 #pragma unroll
       for (int h = 0; h < C::NH; ++h) {
         const int u = t * C::NH + h;
         const uint32_t lim = (u == 0 && (args.flags & VC_DEBUG_TIMEOUT)) ? 0u : kWaitLimit;
         if (!warp_wait(&s_full[g], u & 1, lim, abort_flag)) {
           record_failure(args.status, abort_flag, kStatusTimeoutS);
-          ok = false;
-          break;
+          return false;
         }
         tc_fence_after();
         uint32_t sr[C::SW];
@@ -375,11 +376,20 @@ __global__ void __launch_bounds__(352, 1) vc_fwd2_kernel(const __grid_constant__
         for (int c0 = 0; c0 < C::SW; c0 += 32) tmem_ld32(tS + c0, *reinterpret_cast<uint32_t(*)[32]>(&sr[c0]));
         tmem_wait_ld();
         tc_fence_before();
-        mbar_arrive(&s_free[g]);  // the next sub-tile may overwrite the score buffer
+        mbar_arrive(&s_free[g]);
 #pragma unroll
         for (int c = 0; c < C::SW; ++c) s[h * C::SW + c] = __uint_as_float(sr[c]);
       }
-      if (!ok) break;
+      return true;
+    };
+    float sk_next = skh[tile_at(0, start)];
+    for (int t = 0; ok && t < nkb; ++t) {
+      if (warp_aborted(abort_flag)) { ok = false; break; }
+      const int j = tile_at(t, start);
+      const float sk = sk_next;
+      if (t + 1 < nkb) sk_next = skh[tile_at(t + 1, start)];
+      float s[128];
+      if (!load_scores(t, s)) { ok = false; break; }
       if (j == nkb - 1 && tail_valid < 128) {  // keys past S: -inf for the max, code 0
 #pragma unroll
         for (int c = 0; c < 128; ++c)
@@ -456,9 +466,41 @@ __global__ void __launch_bounds__(352, 1) vc_fwd2_kernel(const __grid_constant__
       mbar_arrive(&p_full[g]);
     }
 
+    // Repair tiles (V residual repair): the running max is final, so there is no tile max, rescale or
+    // flush; the codes are clipped at 120 (a copied key may score slightly above M), and the zero
+    // one-hot rows keep them out of W and l.
+    if constexpr (kRepair) {
+      const float* skr = args.krep_scales + (int64_t)bh * args.nrt;
+      const float bb = __fsub_rn(kB0, Mrun);
+      const uint64_t b2 = pack2f(bb, bb);
+      for (int t = nkb; ok && t < ntiles; ++t) {
+        if (warp_aborted(abort_flag)) { ok = false; break; }
+        const float aj = aq * skr[t - nkb];
+        float s[128];
+        if (!load_scores(t, s)) { ok = false; break; }
+        const uint64_t a2 = pack2f(aj, aj);
+        uint32_t pk[32];
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          if constexpr (kExpCast) {
+            pk[q] = __vminu4(expcast4(s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3], a2, a2, b2, b2), 0x78787878u);
+          } else {
+            pk[q] = pack4(expcast_off_code(s[4 * q], aj, bb), expcast_off_code(s[4 * q + 1], aj, bb),
+                          expcast_off_code(s[4 * q + 2], aj, bb), expcast_off_code(s[4 * q + 3], aj, bb));
+          }
+        }
+        if (!wait_o(t - 1)) { ok = false; break; }
+        tmem_st16(tP, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
+        tmem_st16(tP + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]));
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&p_full[g]);
+      }
+    }
+
     // Every PV of this group done: the last run's row sums and means, then O = sV A / l (with
     // per-channel scales O[:, d] = s_d A[:, d] / l).
-    if (ok && !warp_aborted(abort_flag) && wait_o(nkb - 1)) {
+    if (ok && !warp_aborted(abort_flag) && wait_o(ntiles - 1)) {
       float w[16];
       read_w(w);
       float ws = 0.f;
@@ -471,7 +513,7 @@ __global__ void __launch_bounds__(352, 1) vc_fwd2_kernel(const __grid_constant__
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&f_full[g]);
-        ready = wait_o(nkb);
+        ready = wait_o(ntiles);
       }
       if (ready && qt < nkb) {
         const float scale = svch ? 1.f / lf : sv / lf;
@@ -512,13 +554,13 @@ __global__ void __launch_bounds__(352, 1) vc_fwd2_kernel(const __grid_constant__
   }
 }
 
-template <int D, bool kExpCast>
+template <int D, bool kExpCast, bool kRepair>
 static int launch_fwd2(const PlanBuffers& p, const FwdMaps& maps, uint16_t* O, unsigned flags, cudaStream_t st) {
   using C = Fwd2Cfg<D>;
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(vc_fwd2_kernel<D, kExpCast>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(vc_fwd2_kernel<D, kExpCast, kRepair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM) != cudaSuccess)
       return VC_ERR_CUDA;
     attr_set = true;
   }
@@ -529,26 +571,29 @@ static int launch_fwd2(const PlanBuffers& p, const FwdMaps& maps, uint16_t* O, u
   a.vscales_ch = p.has_vchannel ? p.vscales_ch : nullptr;
   a.out = O;
   a.status = p.status;
-  a.krep_scales = nullptr;
+  a.krep_scales = p.krep_scales;
   a.S = p.S;
   a.S_pad = p.S_pad;
   a.nkb = p.nkb;
-  a.nrt = 0;
-  a.R_pad = 0;
+  a.nrt = p.nrt;
+  a.R_pad = p.R_pad;
   a.flags = flags;
   a.code_scale = (float)(8.0 * 1.4426950408889634 / __builtin_sqrt((double)D));
   a.use_mean = (p.has_means && (flags & VC_VSMOOTH)) ? 1 : 0;
+  if (a.use_mean && a.nrt > 0) return VC_ERR_INVALID_ARG;  // repair rows exist only without means
   dim3 grid((p.nkb + 1) / 2, p.B * p.H);
-  vc_fwd2_kernel<D, kExpCast><<<grid, 352, C::SMEM, st>>>(maps, a);
+  vc_fwd2_kernel<D, kExpCast, kRepair><<<grid, 352, C::SMEM, st>>>(maps, a);
   return cudaPeekAtLastError() == cudaSuccess ? VC_OK : VC_ERR_CUDA;
 }
 
-// Used for D = 64 (no repair tiles). The kernel also builds for D = 128 with score half-tiles, but
-// there the one-query-tile kernel is faster (59.1 against 71.8 ms on the 40-head, 75600-token case).
+// Used for D = 64. The kernel also builds for D = 128 with score half-tiles, but there the one-query-tile
+// kernel is faster (59.1 against 71.8 ms on the 40-head, 75600-token case).
 int forward2_launch(const PlanBuffers& p, const FwdMaps& maps, uint16_t* O, unsigned flags, cudaStream_t st) {
   if (p.D != 64) return VC_ERR_UNSUPPORTED;
   const bool ec = (flags & VC_EXPCAST) != 0;
-  return ec ? launch_fwd2<64, true>(p, maps, O, flags, st) : launch_fwd2<64, false>(p, maps, O, flags, st);
+  if (p.nrt > 0)
+    return ec ? launch_fwd2<64, true, true>(p, maps, O, flags, st) : launch_fwd2<64, false, true>(p, maps, O, flags, st);
+  return ec ? launch_fwd2<64, true, false>(p, maps, O, flags, st) : launch_fwd2<64, false, false>(p, maps, O, flags, st);
 }
 
 }  // namespace vc
