@@ -69,3 +69,68 @@ def test_l1344_fullsize(m):
 @pytest.mark.parametrize("name", ["sweep_d64_s4096", "sweep_d128_s16384", "sweep_d64_s65536", "sweep_d128_s131072"])
 def test_sweep_points(m, name):
     check_fullsize(m, synth.config(name), rows_per_head=3, prep_heads=(1,))
+
+
+def test_wan_fullsize_repair(m):
+    """The Open-VC configuration at the benchmark size: no V-Smooth, one V scale per head, the 0.5% of
+    tokens with the largest residual energy repaired ("Open-VC Attention", "Why V residual repair").
+    Selection, copied keys and repair codes bit-exact on two heads; sampled rows of every head within
+    the acceptance bound of the oracle run on the GPU's plan."""
+    cfg = synth.config("wan")
+    S, H = cfg["S"], cfg["H"]
+    n = m.repair_rows_for(S, 0.005)
+    Q, K, V = synth.make_inputs(cfg, seed=1, device="cuda")
+    plan = m.vc_attn_prepare_repair(Q, K, V, n)
+    O = m.vc_attn_forward(plan, flags=m.VC_EXPCAST | m.VC_MIDWINDOW)
+    torch.cuda.synchronize()
+    assert m.vc_plan_status(plan)[0] == 0
+    allp = gpu_plan_all(m, plan)
+    get = lambda what: m.vc_plan_get(plan, what).cpu().numpy()
+    idx, kc, sk, vt = (get(w) for w in (m.VC_PLAN_REPAIR_IDX, m.VC_PLAN_REPAIR_KCODES, m.VC_PLAN_REPAIR_KSCALES,
+                                        m.VC_PLAN_REPAIR_VCODES))
+    rng = np.random.default_rng(11)
+    for h in range(H):
+        g = head_of(allp, 0, h)
+        rep = {"n": n, "kc": kc[0, h], "sk": sk[0, h], "rc": vt[0, h].T}
+        if h in (0, 17):
+            o = oracle.prepare_head(u16(Q[0, h]), u16(K[0, h]), u16(V[0, h]), 1, 1, vsmooth=False, n_repair=n)
+            compare_prep(g, o, S)
+            for key, want in (("idx", o["repair"]["idx"]), ("kc", o["repair"]["kc"]), ("sk", o["repair"]["sk"]),
+                              ("rc", o["repair"]["rc"])):
+                got = idx[0, h] if key == "idx" else rep[key]
+                assert np.array_equal(got, want), f"head {h}: repair {key}"
+        rows = np.unique(np.concatenate([rng.choice(S, 6, replace=False), [S - 1]]))
+        ref = oracle.attention_quant(g["qc"], g["sq"], g["kc"], g["sk"], g["rc"], g["sv"], None, S, rows, repair=rep)[0]
+        assert_within(f64(O[0, h])[rows], ref, float(np.abs(f64(V[0, h])).max()), f"repair head {h}")
+    plan.destroy()
+
+
+def test_wan_fullsize_channel_scale_and_k_centering(m):
+    """V-Smooth with one V scale per channel and centred keys at the benchmark size: prepare outputs
+    bit-exact on one head (the oracle fed the GPU's permutation), sampled rows of every head."""
+    cfg = synth.config("wan")
+    S, H = cfg["S"], cfg["H"]
+    Q, K, V = synth.make_inputs(cfg, seed=2, device="cuda")
+    plan = m.vc_attn_prepare_ex(Q, K, V, cfg["k"], cfg["iters"],
+                                flags=m.VC_VSMOOTH | m.VC_VSCALE_CHANNEL | m.VC_KCENTER)
+    O = m.vc_attn_forward(plan)
+    torch.cuda.synchronize()
+    assert m.vc_plan_status(plan)[0] == 0
+    allp = gpu_plan_all(m, plan)
+    svc = m.vc_plan_get(plan, m.VC_PLAN_VCHSCALES).cpu().numpy()
+    mt = u16(m.vc_plan_get(plan, m.VC_PLAN_MEANS_T))
+    nkb = (S + 127) // 128
+    rng = np.random.default_rng(12)
+    for h in range(H):
+        g = head_of(allp, 0, h)
+        if h == 5:
+            o = oracle.prepare_head(u16(Q[0, h]), u16(K[0, h]), u16(V[0, h]), cfg["k"], cfg["iters"], perm=g["perm"],
+                                    kcenter=True, vscale_channel=True)
+            for key in ("qc", "sq", "kc", "sk", "mub", "rc"):
+                assert np.array_equal(g[key], o[key]), f"head {h}: {key}"
+            assert np.array_equal(svc[0, h], o["sv"]) and np.array_equal(mt[0, h, :, :nkb].T, o["mut"])
+        rows = np.unique(np.concatenate([rng.choice(S, 6, replace=False), [0]]))
+        ref = oracle.attention_quant(g["qc"], g["sq"], g["kc"], g["sk"], g["rc"], svc[0, h], g["mub"], S, rows,
+                                     mut=mt[0, h, :, :nkb].T)[0]
+        assert_within(f64(O[0, h])[rows], ref, float(np.abs(f64(V[0, h])).max()), f"channel head {h}")
+    plan.destroy()
