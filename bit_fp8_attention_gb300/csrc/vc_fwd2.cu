@@ -314,8 +314,13 @@ __global__ void __launch_bounds__(352, 1) vc_fwd2_kernel(const __grid_constant__
     }
     if (ok && use_mean && !warp_aborted(abort_flag)) {  // the last block run: F arrives after the loops
       for (int g = 0; g < 2; ++g) {
-        if (!warp_wait(&f_full[g], 0, kWaitLimit, abort_flag) || (tc_fence_after(), !issue_mean(g, seg))) {
+        if (!warp_wait(&f_full[g], 0, kWaitLimit, abort_flag)) {
           fail(kStatusTimeoutP);
+          break;
+        }
+        tc_fence_after();
+        if (!issue_mean(g, seg)) {
+          fail(kStatusTimeoutLoad);
           break;
         }
         if (leader) mma_commit(&o_done[g]);  // phase nkb of the group's o_done
