@@ -197,19 +197,23 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else if (warp == 9) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(128, C::CH);
-      const uint64_t dx0 = smem_desc(sX, 1024, kSw128);
-      const uint64_t dc0 = smem_desc(sC, 1024, kSw128);
-      bool ok = wait_or_abort(x_full, 0, abort_flag);
-      for (int ch = 0; ok && ch < nch; ++ch) {
-        const int s = ch % C::NST, b = ch & 1;
-        if (!wait_or_abort(&c_full[s], (ch / C::NST) & 1, abort_flag) ||
-            !wait_or_abort(&acc_empty[b], ((ch >> 1) & 1) ^ 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+    // The whole warp runs the schedule (waits voted, so it stays converged); one elected lane issues.
+    const bool leader = elect_one();
+    constexpr uint32_t idesc = idesc_bf16(128, C::CH);
+    const uint64_t dx0 = smem_desc(sX, 1024, kSw128);
+    const uint64_t dc0 = smem_desc(sC, 1024, kSw128);
+    auto wwait = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, wait_or_abort(bar, parity, abort_flag));
+    };
+    bool ok = wwait(x_full, 0);
+    for (int ch = 0; ok && ch < nch; ++ch) {
+      const int s = ch % C::NST, b = ch & 1;
+      if (!wwait(&c_full[s], (ch / C::NST) & 1) || !wwait(&acc_empty[b], ((ch >> 1) & 1) ^ 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (leader) {
 #pragma unroll
         for (int g = 0; g < C::TPC; ++g) {
           const uint32_t d = tmem + (uint32_t)((g * 2 + b) * C::CH);
@@ -228,10 +232,12 @@ __global__ void __launch_bounds__(320, 1)
         mma_commit(&c_empty[s]);
         mma_commit(&acc_full[b]);
       }
-      if (!ok) fail(status, abort_flag);
-      mma_commit(drain);
-      if (!mbar_wait(drain, 0, kWaitLimit)) fail(status, abort_flag);
+      __syncwarp();
     }
+    if (!ok && lane == 0) fail(status, abort_flag);
+    if (leader) mma_commit(drain);
+    __syncwarp();
+    if (!__all_sync(0xffffffffu, mbar_wait(drain, 0, kWaitLimit)) && lane == 0) fail(status, abort_flag);
   } else {
     // ---------------------------------------------------------------- argmin epilogue, warps 0-7
     const int g = warp >> 2, wq = warp & 3;
@@ -251,28 +257,28 @@ __global__ void __launch_bounds__(320, 1)
         break;
       }
       tc_fence_after();
-#pragma unroll 1
-      for (int c0 = 0; c0 < C::CH; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(tbase + (uint32_t)(b * C::CH + c0), r);
-        tmem_wait_ld();
-        const float4* cn4 = reinterpret_cast<const float4*>(cn + ch * C::CH + c0);
+      // All 128 dot products of the chunk in one round trip; the buffer is released before the scan.
+      uint32_t r[C::CH];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float4 n4 = __ldg(cn4 + q);
-          const float nn[4] = {n4.x, n4.y, n4.z, n4.w};
+      for (int c0 = 0; c0 < C::CH; c0 += 32)
+        tmem_ld32(tbase + (uint32_t)(b * C::CH + c0), *reinterpret_cast<uint32_t(*)[32]>(&r[c0]));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&acc_empty[b]);
+      const float4* cn4 = reinterpret_cast<const float4*>(cn + ch * C::CH);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float dist = fmaf(-2.f, __uint_as_float(r[4 * q + e]), nn[e]);
-            if (dist < best) {  // ascending scan: a tie keeps the lower index
-              best = dist;
-              bi = ch * C::CH + c0 + 4 * q + e;
-            }
+      for (int q = 0; q < C::CH / 4; ++q) {
+        const float4 n4 = __ldg(cn4 + q);
+        const float nn[4] = {n4.x, n4.y, n4.z, n4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float dist = fmaf(-2.f, __uint_as_float(r[4 * q + e]), nn[e]);
+          if (dist < best) {  // ascending scan: a tie keeps the lower index
+            best = dist;
+            bi = ch * C::CH + 4 * q + e;
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive(&acc_empty[b]);
     }
     if (ok && tok < S) labels[(int64_t)bh * S + tok] = bi;
   }
