@@ -56,6 +56,20 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The slowest rank's time: every replica does the same work, so the job ends with the last one."""
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_replica: float, world: int, ms_per_step: float) -> float:
+    """Replicas only (weak scaling): all ranks' work over the slowest rank's step time."""
+    return world * flops_per_replica / (ms_per_step * 1e-3) / 1e12
+
+
 def workload_name(cfg):
     return (f"{cfg['name']}: B={cfg['B']} H={cfg['H']} S={cfg['S']} D={cfg['D']} "
             f"grid={'x'.join(map(str, cfg['grid']))} k={cfg['k']} iters={cfg['iters']}")
@@ -280,12 +294,9 @@ def main():
         barrier()
     ms_total = t_start.elapsed_time(t_end)
     fwd_ms = [a.elapsed_time(b) for a, b in fwd_events]
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, world, dev)
     ms_step = ms_total / args.steps
-    value = world * flops / (ms_step * 1e-3) / 1e12
+    value = whole_job_tflops(flops, world, ms_step)
     clocks = clk.summary()
 
     # Prepare split (untimed for `value`): quantisation/gather/means with the permutation given,
@@ -390,9 +401,9 @@ def main():
         b.record(s_out)
         torch.cuda.synchronize()
         barrier()
-        e2e_ms = a.elapsed_time(b) / n_e2e
+        e2e_ms = max_over_ranks(a.elapsed_time(b) / n_e2e, world, dev)
         nbytes = Q.numel() * Q.element_size()
-        e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+        e2e = {"value": whole_job_tflops(flops, world, e2e_ms), "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": 3 * nbytes, "d2h_bytes_per_step": nbytes,
                "copies": "own streams, double-buffered: step i+1's inputs and step i-1's output move while step i "
                          "computes"}
