@@ -45,6 +45,8 @@ def plan_repair(m, plan):
     (2049, 128, 200, "kcenter"),       # two repair tiles, copied keys centred
     (1000, 128, 130, "channel"),       # per-channel residual scales
     (300, 64, 300, 0),                 # every token repaired
+    (1, 64, 1, 0),                     # one token: one key tile and one repair tile
+    (129, 128, 129, "channel"),        # two ragged key tiles, two repair tiles, every token repaired
 ])
 def test_repair_parity(m, S, D, n, flags):
     H = 2
