@@ -33,6 +33,12 @@ int check_device() {
   return (major == 10 && minor == 3) ? VC_OK : VC_ERR_NO_DEVICE;
 }
 
+// A plan's buffers and tensor maps live on the device that was current when it was created.
+bool on_plan_device(const vc_plan* plan) {
+  int cur = -1;
+  return cudaGetDevice(&cur) == cudaSuccess && cur == plan->device;
+}
+
 int check_shape(int B, int H, int S, int D, int k) {
   if (B < 1 || H < 1 || S < 1 || k < 1) return VC_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return VC_ERR_UNSUPPORTED;
@@ -153,6 +159,7 @@ int prepare_impl(const void* Q, const void* K, const void* V, int B, int H, int 
   rc = check_device();
   if (rc != VC_OK) return rc;
   if (*plan) {
+    if (!on_plan_device(*plan)) return VC_ERR_INVALID_ARG;
     const vc::PlanBuffers& b = (*plan)->b;
     if (b.B != B || b.H != H || b.S != S || b.D != D || b.k != k_clusters || b.nrep != n_repair)
       return VC_ERR_PLAN_MISMATCH;
@@ -197,6 +204,7 @@ int vc_attn_forward(const vc_plan* plan, void* O, unsigned flags, cudaStream_t s
   if (!plan || !O || !aligned16(O)) return VC_ERR_INVALID_ARG;
   const unsigned known = VC_EXPCAST | VC_VSMOOTH | VC_MIDWINDOW | VC_DEBUG_TIMEOUT;
   if (flags & ~known) return VC_ERR_INVALID_ARG;
+  if (!on_plan_device(plan)) return VC_ERR_INVALID_ARG;
   return vc::forward_launch(plan->b, plan->maps, (uint16_t*)O, flags, stream);
 }
 

@@ -740,13 +740,8 @@ int encode_fwd_maps(const PlanBuffers& p, FwdMaps* maps) {
 template <int D, bool kExpCast, bool kRepair>
 static int launch_fwd(const PlanBuffers& p, const FwdMaps& maps, uint16_t* O, unsigned flags, cudaStream_t st) {
   using C = FwdCfg<D>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(vc_fwd_kernel<D, kExpCast, kRepair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM) != cudaSuccess)
-      return VC_ERR_CUDA;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  if (ensure_smem_attr(vc_fwd_kernel<D, kExpCast, kRepair>, C::SMEM, attr_done) != VC_OK) return VC_ERR_CUDA;
   FwdArgs a;
   a.qscales = p.qscales;
   a.kscales = p.kscales;

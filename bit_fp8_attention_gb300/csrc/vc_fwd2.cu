@@ -562,13 +562,8 @@ __global__ void __launch_bounds__(352, 1) vc_fwd2_kernel(const __grid_constant__
 template <int D, bool kExpCast, bool kRepair>
 static int launch_fwd2(const PlanBuffers& p, const FwdMaps& maps, uint16_t* O, unsigned flags, cudaStream_t st) {
   using C = Fwd2Cfg<D>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(vc_fwd2_kernel<D, kExpCast, kRepair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM) != cudaSuccess)
-      return VC_ERR_CUDA;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  if (ensure_smem_attr(vc_fwd2_kernel<D, kExpCast, kRepair>, C::SMEM, attr_done) != VC_OK) return VC_ERR_CUDA;
   FwdArgs a;
   a.qscales = p.qscales;
   a.kscales = p.kscales;

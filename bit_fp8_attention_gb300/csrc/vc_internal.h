@@ -4,9 +4,24 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "vc_attn.h"
 
 namespace vc {
+
+// Opt a kernel into its dynamic shared memory size once per device (the attribute is per device, and
+// setting it again is harmless, so concurrent first calls need no lock).
+template <typename Kernel>
+int ensure_smem_attr(Kernel* fn, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return VC_ERR_CUDA;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (done.load(std::memory_order_relaxed) & bit) return VC_OK;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return VC_ERR_CUDA;
+  done.fetch_or(bit, std::memory_order_relaxed);
+  return VC_OK;
+}
 
 // Device buffers of a plan (layouts as documented in vc_attn.h).
 struct PlanBuffers {

@@ -480,13 +480,8 @@ template <int D>
 int launch_kmeans(const PlanBuffers& p, const uint16_t* V, int iters, bool warm, cudaStream_t st) {
   using C = AsgCfg<D>;
   const int BH = p.B * p.H, S = p.S, k = p.k, kpad = p.kpad;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(kmeans_assign_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
-        cudaSuccess)
-      return VC_ERR_CUDA;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  if (ensure_smem_attr(kmeans_assign_kernel<D>, C::SMEM, attr_done) != VC_OK) return VC_ERR_CUDA;
   CUtensorMap xmap, cmap;
   int rc = encode_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t*>(V), D, (uint64_t)BH * S,
                      (uint64_t)D * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);

@@ -93,7 +93,9 @@ enum {
  * block, the E4M3 codes of the V' residual stored transposed and zero-padded as [B, H, D, S_pad]
  * (key dimension contiguous, the layout of the PV operand) with one fp32 scale per head, the
  * bf16 128-row block means, the k-means labels and centroids, and a device status word.
- * S_pad = 128 * ceil(S/128).  The library owns these buffers until vc_plan_destroy().        */
+ * S_pad = 128 * ceil(S/128).  The library owns these buffers until vc_plan_destroy().
+ * A plan belongs to the device that was current when it was created: preparing into it or running
+ * the forward with another current device returns VC_ERR_INVALID_ARG.                         */
 typedef struct vc_plan vc_plan;
 
 /* vc_attn_prepare
