@@ -101,3 +101,15 @@ def test_invalid_arguments_rejected_without_device(L):
     L.vc_plan_destroy(None)
     assert L.vc_expcast_encode(None, None, None, 5, None, None) == -1
     assert L.vc_expcast_encode(None, None, None, -1, None, None) == -1
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    """No fallback: without the built library every call raises instead of computing anything."""
+    import bit_fp8_attention_gb300 as vc
+
+    monkeypatch.setattr(vc, "_lib", None)
+    monkeypatch.setattr(vc, "LIB_PATH", str(tmp_path / "absent.so"))
+    with pytest.raises(ImportError):
+        vc.lib()
+    with pytest.raises(ImportError):
+        vc.vc_schedule_action(0, 40, 4)
