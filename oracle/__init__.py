@@ -30,6 +30,7 @@ _lib = None
 BLOCK = 128
 EXPCAST = 1
 MIDWINDOW = 2
+HADAMARD = 4  # Q and K were rotated (reading R19)
 
 
 def build(force: bool = False) -> str:
@@ -71,6 +72,9 @@ def lib():
             "orc_expcast_of_u": (ctypes.c_int, [ctypes.c_double]),
             "orc_quant_blocks": (None, [u16, ctypes.c_int64, ctypes.c_int, u8, f32]),
             "orc_quant_blocks_centered": (None, [u16, ctypes.c_int64, ctypes.c_int, u16, u8, f32]),
+            "orc_quant_blocks_rot": (None, [u16, ctypes.c_int64, ctypes.c_int, u16, ctypes.c_int, u8, f32]),
+            "orc_fwht_f32": (None, [f32, ctypes.c_int]),
+            "orc_code_scale_rot": (ctypes.c_float, [ctypes.c_int]),
             "orc_kmeans_from": (None, [u16, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, i32, f64, f64]),
             "orc_schedule_action": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
             "orc_channel_mean_bf16": (None, [u16, ctypes.c_int64, ctypes.c_int, u16]),
@@ -197,10 +201,11 @@ def code_scale(D: int) -> float:
 # ----------------------------------------------------------------------------------------------
 # Preparation steps
 # ----------------------------------------------------------------------------------------------
-def quant_blocks(x, center=None) -> tuple[np.ndarray, np.ndarray]:
+def quant_blocks(x, center=None, rotate: bool = False) -> tuple[np.ndarray, np.ndarray]:
     """Per-128-token block E4M3 quantisation ([OVC] "Scheduling around ExpCast").
 
-    x: [S, D] bf16. center: None, or [D] bf16 subtracted (fp32) from every row first.
+    x: [S, D] bf16. center: None, or [D] bf16 subtracted (fp32) from every row first. rotate: apply
+    the fp32 Walsh-Hadamard butterfly to every row first (reading R19, see fwht).
     Returns codes [S_pad, D] uint8 and scales [nkb] float32.
     """
     x = _u16(x)
@@ -209,10 +214,18 @@ def quant_blocks(x, center=None) -> tuple[np.ndarray, np.ndarray]:
     codes = np.empty((nkb * BLOCK, D), dtype=np.uint8)
     scales = np.empty(nkb, dtype=np.float32)
     c = None if center is None else np.ascontiguousarray(_u16(center).reshape(D))
-    lib().orc_quant_blocks_centered(_ptr(x, ctypes.c_uint16), S, D,
-                                    None if c is None else _ptr(c, ctypes.c_uint16),
-                                    _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_float))
+    lib().orc_quant_blocks_rot(_ptr(x, ctypes.c_uint16), S, D, None if c is None else _ptr(c, ctypes.c_uint16),
+                               1 if rotate else 0, _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_float))
     return codes, scales
+
+
+def fwht(x) -> np.ndarray:
+    """The unnormalised Walsh-Hadamard transform of each row of x, as the fp32 butterfly of reading R19."""
+    a = np.array(x, dtype=np.float32, order="C", copy=True)  # never the caller's array
+    rows = a.reshape(-1, a.shape[-1])
+    for r in rows:
+        lib().orc_fwht_f32(_ptr(r, ctypes.c_float), r.size)
+    return a
 
 
 def channel_mean_bf16(x) -> np.ndarray:
@@ -392,13 +405,14 @@ def repair_select(v, amax, n_rep: int):
     return idx[:n_rep], energy[:S], rep[:nkb_of(n_rep) * BLOCK]
 
 
-def repair_rows(k, v, amax, n_rep: int, kcenter=None) -> dict:
+def repair_rows(k, v, amax, n_rep: int, kcenter=None, rotate: bool = False) -> dict:
     """The repair rows of one head: the selected tokens, their keys copied and quantised as extra
-    128-row blocks (minus the K centre when given), and their residual codes."""
+    128-row blocks (minus the K centre when given, rotated like every key when asked), and their
+    residual codes."""
     idx, energy, rep = repair_select(v, amax, n_rep)
     out = {"n": int(n_rep), "idx": idx, "energy": energy, "rc": rep}
     if n_rep > 0:
-        out["kc"], out["sk"] = quant_blocks(_u16(k)[idx], center=kcenter)
+        out["kc"], out["sk"] = quant_blocks(_u16(k)[idx], center=kcenter, rotate=rotate)
     else:
         out["kc"], out["sk"] = np.zeros((0, _u16(k).shape[1]), dtype=np.uint8), np.zeros(0, dtype=np.float32)
     return out
@@ -433,7 +447,8 @@ def attention_demeaned_exact(q, k, v, rows, midwindow: bool = True) -> np.ndarra
 # Whole-path conveniences for one batch-head
 # ----------------------------------------------------------------------------------------------
 def prepare_head(q, k, v, k_clusters: int, iters: int, vsmooth: bool = True, perm=None,
-                 kcenter: bool = False, vscale_channel: bool = False, n_repair: int = 0) -> dict:
+                 kcenter: bool = False, vscale_channel: bool = False, n_repair: int = 0,
+                 hadamard: bool = False) -> dict:
     """Everything the prepare step produces for one batch-head, computed on the CPU.
 
     vsmooth=False: identity permutation, no means (R = V). perm given: use it instead of k-means
@@ -441,6 +456,7 @@ def prepare_head(q, k, v, k_clusters: int, iters: int, vsmooth: bool = True, per
     kcenter: subtract the keys' channel mean before their quantisation (see channel_mean_bf16).
     vscale_channel: one residual scale per channel instead of one per head (see demean).
     n_repair: V residual repair rows (without V-Smooth only; see repair_rows).
+    hadamard: rotate Q and K rows before their quantisation (reading R19, see fwht).
     """
     assert n_repair == 0 or not vsmooth, "V residual repair is defined without V-Smooth"
     q, k, v = _u16(q), _u16(k), _u16(v)
@@ -455,25 +471,26 @@ def prepare_head(q, k, v, k_clusters: int, iters: int, vsmooth: bool = True, per
         perm = np.arange(S, dtype=np.int32)
     perm = np.asarray(perm, dtype=np.int32)
     out["perm"] = perm
-    out["qc"], out["sq"] = quant_blocks(q)
+    out["qc"], out["sq"] = quant_blocks(q, rotate=hadamard)
     kp = gather_rows(k, perm)
     kmu = channel_mean_bf16(k) if kcenter else None
     out["kmu"] = kmu
-    out["kc"], out["sk"] = quant_blocks(kp, center=kmu)
+    out["kc"], out["sk"] = quant_blocks(kp, center=kmu, rotate=hadamard)
     dm = demean(v, perm, subtract_mean=vsmooth, per_channel=vscale_channel)
     out.update(rc=dm["rc"], sv=dm["sv"], amax=dm["amax"], mub=dm["mub"], mu=dm["mu"], resid=dm["resid"],
                mut=dm.get("mut"))
     out["vsmooth"] = vsmooth
     out["vscale_channel"] = vscale_channel
+    out["hadamard"] = hadamard
     out["repair"] = None
     if n_repair > 0:
         amax = dm["amax"] if vscale_channel else np.full(D, dm["amax"], dtype=np.float32)
-        out["repair"] = repair_rows(k, v, amax, n_repair, kcenter=kmu)
+        out["repair"] = repair_rows(k, v, amax, n_repair, kcenter=kmu, rotate=hadamard)
     return out
 
 
 def forward_head(prep: dict, rows, expcast: bool = True, midwindow: bool = True):
-    flags = (EXPCAST if expcast else 0) | (MIDWINDOW if midwindow else 0)
+    flags = (EXPCAST if expcast else 0) | (MIDWINDOW if midwindow else 0) | (HADAMARD if prep.get("hadamard") else 0)
     mub = prep["mub"] if prep["vsmooth"] else None
     return attention_quant(prep["qc"], prep["sq"], prep["kc"], prep["sk"], prep["rc"], prep["sv"], mub,
                            prep["S"], rows, flags, mut=prep.get("mut") if prep["vsmooth"] else None,

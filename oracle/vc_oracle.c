@@ -37,6 +37,9 @@
  *       into extra 128-row blocks quantised like any other key block (own scale per block); their
  *       residuals are coded in E4M3 in the main residual codes' units; repair tiles leave the running
  *       max and the row sum alone (codes clip at 120).  Defined without V-Smooth only.
+ *   R19 QK Hadamard rotation (an option): the unnormalised Walsh-Hadamard transform of every Q and K
+ *       row (after the K centre), as an fp32 butterfly in a fixed stage order, before the block
+ *       quantiser; the score constant takes the 1/D.
  */
 #include <math.h>
 #include <stdint.h>
@@ -158,30 +161,59 @@ int orc_expcast_of_u(double u) {
  * ------------------------------------------------------------------------------------------- */
 /* center: NULL, or one bf16 value per channel subtracted (in fp32) from every row before the
  * block maximum and the codes are taken (the K channel centering below). */
-void orc_quant_blocks_centered(const uint16_t* x, int64_t S, int D, const uint16_t* center, uint8_t* codes,
-                               float* scales) {
+/* QK Hadamard rotation ([VC] §3.4 "Fused preprocessing", App. B: the Q and K quantisation passes fuse
+ * a Hadamard rotation; Fig. 3 / §4: it shrinks the probability term and is free in time).  Reading R19:
+ * the unnormalised Sylvester-order Walsh-Hadamard transform of each row, y = H_D x with
+ * H_D[i][j] = (-1)^popcount(i & j), computed in fp32 as the usual butterfly: stages s = 1, 2, ..., D/2,
+ * each replacing the pair (x[i], x[i+s]) (bit s of i clear) by (x[i] + x[i+s], x[i] - x[i+s]).  The
+ * 1/sqrt(D) of the orthonormal rotation cancels in the block quantiser's amax scale and is folded into
+ * the score constant instead (scores of rotated operands are D times the plain ones). */
+void orc_fwht_f32(float* x, int D) {
+  for (int s = 1; s < D; s <<= 1)
+    for (int i = 0; i < D; ++i)
+      if (!(i & s)) {
+        float a = x[i], b = x[i + s];
+        x[i] = a + b;
+        x[i + s] = a - b;
+      }
+}
+
+/* Row t of the block quantiser's input in fp32: x - center when a centre is given, then rotated. */
+static void orc_quant_row(const uint16_t* x, int64_t t, int D, const uint16_t* center, int rotate, float* v) {
+  for (int d = 0; d < D; ++d) {
+    v[d] = bf16_to_f32(x[t * D + d]);
+    if (center) v[d] = v[d] - bf16_to_f32(center[d]);
+  }
+  if (rotate) orc_fwht_f32(v, D);
+}
+
+void orc_quant_blocks_rot(const uint16_t* x, int64_t S, int D, const uint16_t* center, int rotate, uint8_t* codes,
+                          float* scales) {
   int64_t nkb = (S + ORC_BLOCK - 1) / ORC_BLOCK;
+  float* v = (float*)malloc((size_t)D * sizeof(float));
   memset(codes, 0, (size_t)(nkb * ORC_BLOCK * D));
   for (int64_t j = 0; j < nkb; ++j) {
     int64_t t0 = j * ORC_BLOCK, t1 = t0 + ORC_BLOCK < S ? t0 + ORC_BLOCK : S;
     float amax = 0.0f;
-    for (int64_t t = t0; t < t1; ++t)
-      for (int d = 0; d < D; ++d) {
-        float v = bf16_to_f32(x[t * D + d]);
-        if (center) v = v - bf16_to_f32(center[d]);
-        v = fabsf(v);
-        if (v > amax) amax = v;
-      }
+    for (int64_t t = t0; t < t1; ++t) {
+      orc_quant_row(x, t, D, center, rotate, v);
+      for (int d = 0; d < D; ++d)
+        if (fabsf(v[d]) > amax) amax = fabsf(v[d]);
+    }
     if (amax == 0.0f) { scales[j] = 1.0f; continue; }
     float inv = 448.0f / amax;
     scales[j] = amax / 448.0f;
-    for (int64_t t = t0; t < t1; ++t)
-      for (int d = 0; d < D; ++d) {
-        float v = bf16_to_f32(x[t * D + d]);
-        if (center) v = v - bf16_to_f32(center[d]);
-        codes[t * D + d] = orc_e4m3_encode(v * inv);
-      }
+    for (int64_t t = t0; t < t1; ++t) {
+      orc_quant_row(x, t, D, center, rotate, v);
+      for (int d = 0; d < D; ++d) codes[t * D + d] = orc_e4m3_encode(v[d] * inv);
+    }
   }
+  free(v);
+}
+
+void orc_quant_blocks_centered(const uint16_t* x, int64_t S, int D, const uint16_t* center, uint8_t* codes,
+                               float* scales) {
+  orc_quant_blocks_rot(x, S, D, center, 0, codes, scales);
 }
 
 void orc_quant_blocks(const uint16_t* x, int64_t S, int D, uint8_t* codes, float* scales) {
@@ -472,13 +504,17 @@ void orc_visit_order(int nkb, int qt, int midwindow, int32_t* order) {
  *   an output rescale, row sum of the decoded FP8 probabilities that feed PV, mid-window order.
  * Inputs (one batch-head): qc,kc,rc [S_pad, D] E4M3 codes (K and R already permuted), sq,sk [nkb],
  * sv the per-head residual scale, mub [nkb, D] bf16 means (NULL: no mean term).
- * flags: 1 = ExpCast (else exponentiate then cast), 2 = mid-window order (else linear).
+ * flags: 1 = ExpCast (else exponentiate then cast), 2 = mid-window order (else linear), 4 = Q and K
+ * rotated (R19).
  * rows: query token indices.  Outputs per row: out [D] fp64 = sv*A/l, l, final max M (code units).
  * ------------------------------------------------------------------------------------------- */
 #define ORC_EXPCAST 1
 #define ORC_MIDWINDOW 2
+#define ORC_HADAMARD 4 /* Q and K were rotated (R19): the score constant carries 1/D more */
 
 float orc_code_scale(int D) { return (float)(8.0 * 1.4426950408889634 / sqrt((double)D)); }
+/* With rotated Q and K (R19) the scores carry a factor D. */
+float orc_code_scale_rot(int D) { return (float)(8.0 * 1.4426950408889634 / ((double)D * sqrt((double)D))); }
 
 /* svc: NULL (one residual scale sv per head, means mub in true units) or [D] per-channel scales with mut
  * the means already divided by them (R17): then the mean term is r_j * mut[j,d] and O[d] = svc[d] A[d] / l. */
@@ -495,7 +531,7 @@ void orc_attention_quant_rep(const uint8_t* qc, const float* sq, const uint8_t* 
                              double* out, double* l_out, float* m_out) {
   int nrt = (int)((n_rep + ORC_BLOCK - 1) / ORC_BLOCK);
   int nkb = (int)((S + ORC_BLOCK - 1) / ORC_BLOCK);
-  float C = orc_code_scale(D);
+  float C = (flags & ORC_HADAMARD) ? orc_code_scale_rot(D) : orc_code_scale(D);
 #pragma omp parallel
   {
     int32_t* order = (int32_t*)malloc((size_t)nkb * sizeof(int32_t));
