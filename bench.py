@@ -316,6 +316,9 @@ def main():
 
     t_prep_full = time_it(lambda: vc.vc_attn_prepare(Q, K, V, cfg["k"], cfg["iters"], plan=plan))
     t_prep_quant = time_it(lambda: vc.vc_attn_prepare_ex(Q, K, V, cfg["k"], cfg["iters"], perm=perm, plan=plan))
+    # the QK Hadamard rotation fused into the Q and K quantisers ("VC-Attention" Sec. 3.4): its prepare cost
+    t_prep_quant_rot = time_it(lambda: vc.vc_attn_prepare_ex(Q, K, V, cfg["k"], cfg["iters"], perm=perm, plan=plan,
+                                                             flags=vc.VC_VSMOOTH | vc.VC_QK_HADAMARD))
     t_group = max(t_prep_full - t_prep_quant, 0.0)
     # The grouping schedule's actions ("VC-Attention" Sec. 3.4, App. A): a warm-started regroup with half
     # the rounds, pi kept with new means, pi kept without means; amortised over the pages' 40-step run.
@@ -430,6 +433,7 @@ def main():
                                                "reuse": t_step[vc.VC_STEP_REUSE], "plain": t_step[vc.VC_STEP_PLAIN]},
                      "prepare_ms_per_step": sched_prepare_ms},
         "repair": repair,
+        "qk_hadamard": {"prepare_quant_ms": t_prep_quant_rot, "prepare_quant_ms_without": t_prep_quant},
         "roofline": {"bound": "tensor", "kernel": forward_kernel_name(cfg["D"]), "achieved": fwd_tflops,
                      "peak": fp8_peak,
                      "unit": "TFLOP/s", "frac": fwd_tflops / fp8_peak, "traffic": profiled_traffic(cfg),

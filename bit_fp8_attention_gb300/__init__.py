@@ -34,6 +34,7 @@ VC_KCENTER = 8
 VC_WARM_START = 16
 VC_REUSE_PERM = 32
 VC_VSCALE_CHANNEL = 64
+VC_QK_HADAMARD = 128
 VC_DEBUG_TIMEOUT = 1 << 16
 VC_FLAGS_DEFAULT = VC_EXPCAST | VC_VSMOOTH | VC_MIDWINDOW
 

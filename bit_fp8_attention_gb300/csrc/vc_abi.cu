@@ -171,6 +171,7 @@ int prepare_impl(const void* Q, const void* K, const void* V, int B, int H, int 
   pl->b.has_means = vsmooth;
   pl->b.has_kcenter = (flags & VC_KCENTER) != 0;
   pl->b.has_vchannel = (flags & VC_VSCALE_CHANNEL) != 0;
+  pl->b.has_hadamard = (flags & VC_QK_HADAMARD) != 0;
   rc = vc::prepare_launch(pl->b, (const uint16_t*)Q, (const uint16_t*)K, (const uint16_t*)V,
                           vsmooth ? perm : nullptr, vsmooth, pl->b.has_kcenter, reuse_perm, warm,
                           pl->b.has_vchannel, iters, stream);

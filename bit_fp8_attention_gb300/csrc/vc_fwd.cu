@@ -756,7 +756,9 @@ static int launch_fwd(const PlanBuffers& p, const FwdMaps& maps, uint16_t* O, un
   a.R_pad = p.R_pad;
   a.krep_scales = p.krep_scales;
   a.flags = flags;
-  a.code_scale = (float)(8.0 * 1.4426950408889634 / __builtin_sqrt((double)D));
+  // 8 log2(e) / sqrt(D); rotated Q and K (Walsh-Hadamard, unnormalised) give D times the scores
+  a.code_scale = (float)(p.has_hadamard ? 8.0 * 1.4426950408889634 / ((double)D * __builtin_sqrt((double)D))
+                                        : 8.0 * 1.4426950408889634 / __builtin_sqrt((double)D));
   a.use_mean = (p.has_means && (flags & VC_VSMOOTH)) ? 1 : 0;
   if (a.use_mean && a.nrt > 0) return VC_ERR_INVALID_ARG;  // repair rows exist only without means
   dim3 grid(p.nkb, p.B * p.H);

@@ -56,6 +56,7 @@ struct PlanBuffers {
   unsigned int* vamax_ch;  // [BH, D] residual |max| of each channel as float bits (per-channel scale)
   float* vscales_ch;    // [BH, D] residual scale of each channel
   bool has_vchannel;    // prepared with one residual scale per channel
+  bool has_hadamard;    // Q and K rows rotated before their quantisation (scores carry a factor D)
   int* status;          // [1]
   bool has_means;       // prepared with V-Smooth
   // V residual repair: n_rep rows per head in nrt = ceil(n_rep/128) extra key tiles (R_pad rows)
@@ -90,7 +91,7 @@ int residual_pack_launch(const uint16_t* V, const int32_t* perm, int BH, int S, 
                          uint8_t* vcodes, float* vscales, unsigned int* amax_scratch, cudaStream_t st);
 // Block quantiser: S rows per head (through perm [BH, S] when given) of a source with S_src rows per head.
 void quant_blocks_launch(const uint16_t* x, const int32_t* perm, const uint16_t* center, int D, int S, int S_pad,
-                         int S_src, int BH, uint8_t* codes, float* scales, cudaStream_t st);
+                         int S_src, int BH, uint8_t* codes, float* scales, cudaStream_t st, bool rotate = false);
 // V residual repair rows (no V-Smooth): energies, selection, copied keys, residual codes. kcen: the K
 // centre or null. The residual maxima (vamax, or vamax_ch when has_vchannel) must be complete.
 int repair_launch(const PlanBuffers& p, const uint16_t* K, const uint16_t* V, const uint16_t* kcen, cudaStream_t st);

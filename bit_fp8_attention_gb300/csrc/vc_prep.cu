@@ -129,10 +129,113 @@ __global__ void __launch_bounds__(256) quant_blocks_kernel(const uint16_t* __res
   }
 }
 
+// The same quantiser with each row rotated first ("VC-Attention", Sec. 3.4 "Fused preprocessing", App. B:
+// the Q and K passes fuse a Hadamard rotation): the unnormalised Walsh-Hadamard transform in fp32, as
+// the butterfly with stages s = 1, 2, ..., D/2 in that order, pair (x[i], x[i+s]) -> (x[i] + x[i+s],
+// x[i] - x[i+s]). A thread holds 8 consecutive channels of a row, so stages 1-4 stay in its registers
+// and stages 8 and up pair it with the lane holding the partner chunk (lane ^ s/8, same row).
+template <int D, bool kCentred>
+__global__ void __launch_bounds__(256) quant_blocks_rot_kernel(const uint16_t* __restrict__ x,
+                                                               const int32_t* __restrict__ perm,
+                                                               const uint16_t* __restrict__ center, int S,
+                                                               int S_pad, int S_src, uint8_t* __restrict__ codes,
+                                                               float* __restrict__ scales) {
+  constexpr int CPR = D / 8;                 // 16-byte chunks per row
+  constexpr int NCH = 128 * CPR / 256;       // chunks per thread
+  static_assert(32 % CPR == 0, "a row's chunks sit in consecutive lanes of one warp");
+  const int j = blockIdx.x, bh = blockIdx.y;
+  const int nkb = S_pad / 128;
+  const uint16_t* xh = x + (int64_t)bh * S_src * D;
+  const int32_t* ph = perm ? perm + (int64_t)bh * S : nullptr;
+  const int cc = threadIdx.x % CPR;          // this thread's chunk of every row it holds
+  __shared__ uint4 cen_s[CPR];
+  __shared__ float red[8];
+  if (kCentred && threadIdx.x < CPR)
+    cen_s[threadIdx.x] = __ldg(reinterpret_cast<const uint4*>(center + (int64_t)bh * D) + threadIdx.x);
+  uint4 v[NCH];
+#pragma unroll
+  for (int m = 0; m < NCH; ++m) {
+    const int t = j * 128 + (threadIdx.x + 256 * m) / CPR;
+    v[m] = make_uint4(0, 0, 0, 0);
+    if (t < S) v[m] = *reinterpret_cast<const uint4*>(xh + (int64_t)(ph ? ph[t] : t) * D + cc * 8);
+  }
+  if (kCentred) __syncthreads();
+  const uint4 cm = kCentred ? cen_s[cc] : make_uint4(0, 0, 0, 0);
+  float y[NCH][8];
+#pragma unroll
+  for (int m = 0; m < NCH; ++m) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) y[m][i] = chunk_elem<kCentred>(v[m], cm, i);
+#pragma unroll
+    for (int s = 1; s < 8; s <<= 1)
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (!(i & s)) {
+          const float a = y[m][i], b = y[m][i + s];
+          y[m][i] = __fadd_rn(a, b);
+          y[m][i + s] = __fsub_rn(a, b);
+        }
+  }
+#pragma unroll
+  for (int s = 8; s < D; s <<= 1) {
+    const int lm = s / 8;                     // partner lane offset
+    const bool lower = (cc & lm) == 0;        // this chunk holds x[i], the partner x[i + s]
+#pragma unroll
+    for (int m = 0; m < NCH; ++m)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float p = __shfl_xor_sync(0xffffffffu, y[m][i], lm);
+        y[m][i] = lower ? __fadd_rn(y[m][i], p) : __fsub_rn(p, y[m][i]);
+      }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int m = 0; m < NCH; ++m) {
+    float a = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(y[m][i]));
+    if (j * 128 + (threadIdx.x + 256 * m) / CPR < S) amax = fmaxf(amax, a);  // pad rows do not count
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+  const bool zero = !(amax > 0.f);
+  const float inv = zero ? 0.f : __fdiv_rn(448.f, amax);
+  if (threadIdx.x == 0) scales[(int64_t)bh * nkb + j] = zero ? 1.f : __fdiv_rn(amax, 448.f);
+  uint8_t* ch = codes + ((int64_t)bh * S_pad + (int64_t)j * 128) * D;
+#pragma unroll
+  for (int m = 0; m < NCH; ++m) {
+    const int r = (threadIdx.x + 256 * m) / CPR;
+    uint32_t lo = 0, hi = 0;
+    if (!zero && j * 128 + r < S) {
+      uint32_t w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) w[q] = cvt_e4m3x2(__fmul_rn(y[m][2 * q], inv), __fmul_rn(y[m][2 * q + 1], inv));
+      lo = w[0] | (w[1] << 16);
+      hi = w[2] | (w[3] << 16);
+    }
+    *reinterpret_cast<uint2*>(ch + (int64_t)r * D + cc * 8) = make_uint2(lo, hi);
+  }
+}
+
 // Launch of the block quantiser for D in {64, 128}, centred or not (grid: S_pad/128 x BH).
 void quant_blocks_launch(const uint16_t* x, const int32_t* perm, const uint16_t* center, int D, int S, int S_pad,
-                         int S_src, int BH, uint8_t* codes, float* scales, cudaStream_t st) {
+                         int S_src, int BH, uint8_t* codes, float* scales, cudaStream_t st, bool rotate) {
   const dim3 grid(S_pad / 128, BH);
+  if (rotate) {
+    if (D == 128) {
+      if (center) quant_blocks_rot_kernel<128, true><<<grid, 256, 0, st>>>(x, perm, center, S, S_pad, S_src, codes, scales);
+      else quant_blocks_rot_kernel<128, false><<<grid, 256, 0, st>>>(x, perm, nullptr, S, S_pad, S_src, codes, scales);
+    } else {
+      if (center) quant_blocks_rot_kernel<64, true><<<grid, 256, 0, st>>>(x, perm, center, S, S_pad, S_src, codes, scales);
+      else quant_blocks_rot_kernel<64, false><<<grid, 256, 0, st>>>(x, perm, nullptr, S, S_pad, S_src, codes, scales);
+    }
+    return;
+  }
   if (D == 128) {
     if (center) quant_blocks_kernel<128, true><<<grid, 256, 0, st>>>(x, perm, center, S, S_pad, S_src, codes, scales);
     else quant_blocks_kernel<128, false><<<grid, 256, 0, st>>>(x, perm, nullptr, S, S_pad, S_src, codes, scales);
@@ -374,7 +477,7 @@ int prepare_launch(const PlanBuffers& p, const uint16_t* Q, const uint16_t* K, c
   const int BH = p.B * p.H, S = p.S, D = p.D, nkb = p.nkb, S_pad = p.S_pad;
   dim3 gblk(nkb, BH);
   // Q: per-block quantisation in token order
-  quant_blocks_launch(Q, nullptr, nullptr, D, S, S_pad, S, BH, p.qcodes, p.qscales, st);
+  quant_blocks_launch(Q, nullptr, nullptr, D, S, S_pad, S, BH, p.qcodes, p.qscales, st, p.has_hadamard);
   if (check_launch()) return VC_ERR_CUDA;
   const int32_t* perm = nullptr;
   if (reuse_perm) {  // the permutation of an earlier prepare stays (grouping schedule)
@@ -410,7 +513,7 @@ int prepare_launch(const PlanBuffers& p, const uint16_t* Q, const uint16_t* K, c
     kstat_mean_kernel<<<(BH * D + 255) / 256, 256, 0, st>>>(p.kexp, p.ksum, S, BH * D, p.kmu);
     kcen = p.kmu;
   }
-  quant_blocks_launch(K, perm, kcen, D, S, S_pad, S, BH, p.kcodes, p.kscales, st);
+  quant_blocks_launch(K, perm, kcen, D, S, S_pad, S, BH, p.kcodes, p.kscales, st, p.has_hadamard);
   // V' = V[pi]: block means, residual maximum per head, residual codes transposed
   if (cudaMemsetAsync(p.vamax, 0, sizeof(unsigned int) * BH, st) != cudaSuccess) return VC_ERR_CUDA;
   unsigned int* ach = vchannel ? p.vamax_ch : nullptr;

@@ -205,7 +205,7 @@ int repair_launch(const PlanBuffers& p, const uint16_t* K, const uint16_t* V, co
   if (D == 128) repair_energy_kernel<128><<<ge, 128, 0, st>>>(V, S, p.vamax, ach, p.energy);
   else repair_energy_kernel<64><<<ge, 128, 0, st>>>(V, S, p.vamax, ach, p.energy);
   repair_select_kernel<<<BH, 1024, 0, st>>>(p.energy, S, p.nrep, p.rep_idx);
-  quant_blocks_launch(K, p.rep_idx, kcen, D, p.nrep, p.R_pad, S, BH, p.krep, p.krep_scales, st);
+  quant_blocks_launch(K, p.rep_idx, kcen, D, p.nrep, p.R_pad, S, BH, p.krep, p.krep_scales, st, p.has_hadamard);
   if (D == 128) repair_vpack_kernel<128><<<gv, 256, 0, st>>>(V, p.rep_idx, S, p.nrep, p.R_pad, p.vamax, ach, p.vrep);
   else repair_vpack_kernel<64><<<gv, 256, 0, st>>>(V, p.rep_idx, S, p.nrep, p.R_pad, p.vamax, ach, p.vrep);
   return cudaPeekAtLastError() == cudaSuccess ? VC_OK : VC_ERR_CUDA;

@@ -81,6 +81,12 @@ enum {
      all-zero channel); codes E4M3(R[t, d] * (448 / amax_d)); forward means bf16(mu / s_d).  The
      forward then computes O[:, d] = s_d * A[:, d] / l. */
   VC_VSCALE_CHANNEL = 64u,
+  /* Prepare only: rotate every Q row and every K row (after the K centre) by the unnormalised
+     Walsh-Hadamard transform before the block quantiser (VC-Attention Sec. 3.4 "Fused preprocessing",
+     App. B: the Q and K passes fuse a Hadamard rotation; QK^T is unchanged since H H^T = D I). Computed
+     in fp32 as the butterfly with stages 1, 2, ..., D/2 in that order; the forward's score constant
+     becomes 8 log2(e) / (D sqrt(D)). */
+  VC_QK_HADAMARD = 128u,
   /* Test hook: the forward kernel's first internal wait gives up at once, so the call reports
      VC_ERR_TIMEOUT through vc_plan_status() without hanging. */
   VC_DEBUG_TIMEOUT = 1u << 16
@@ -122,6 +128,7 @@ int vc_attn_prepare(const void* Q, const void* K, const void* V, int B, int H, i
  * flags: VC_VSMOOTH set -> group (unless perm is given) and demean; clear -> identity
  *   permutation (perm ignored), no means, R = V.  VC_KCENTER set -> subtract the keys' channel
  *   centre before their quantisation.  VC_VSCALE_CHANNEL set -> one residual scale per channel.
+ *   VC_QK_HADAMARD set -> Q and K rows rotated before their quantisation.
  *   VC_WARM_START / VC_REUSE_PERM as documented with the flags.  Other bits are ignored here. */
 int vc_attn_prepare_ex(const void* Q, const void* K, const void* V, int B, int H, int S, int D, int k_clusters,
                        int iters, const int32_t* perm, unsigned flags, cudaStream_t stream, vc_plan** plan);
@@ -140,7 +147,7 @@ int vc_attn_prepare_ex(const void* Q, const void* K, const void* V, int B, int H
  * numerator only.
  * n_repair: 0 <= n_repair <= S rows per head (the pages' operating point is ceil(0.005 * S)); it is
  *   part of the plan's shape (VC_ERR_PLAN_MISMATCH when an existing plan has another count).
- * flags: VC_KCENTER | VC_VSCALE_CHANNEL; VC_VSMOOTH or VC_REUSE_PERM -> VC_ERR_INVALID_ARG.
+ * flags: VC_KCENTER | VC_VSCALE_CHANNEL | VC_QK_HADAMARD; VC_VSMOOTH or VC_REUSE_PERM -> VC_ERR_INVALID_ARG.
  * Other arguments, allocation and asynchrony as vc_attn_prepare. */
 int vc_attn_prepare_repair(const void* Q, const void* K, const void* V, int B, int H, int S, int D, int n_repair,
                            unsigned flags, cudaStream_t stream, vc_plan** plan);

@@ -314,3 +314,32 @@ def test_per_head_plan_reports_equal_channel_scales(m):
     mub = u16(m.vc_plan_get(plan, m.VC_PLAN_MEANS))
     assert np.array_equal(mt[0, 0, :, :6].T, mub[0, 0])  # true units without per-channel scales
     plan.destroy()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("S,D,kcenter", [(3000, 128, False), (2049, 64, True)])
+def test_qk_hadamard(m, S, D, kcenter):
+    """VC_QK_HADAMARD ("VC-Attention", Sec. 3.4 "Fused preprocessing", App. B): Q and K rows rotated by the
+    Walsh-Hadamard butterfly before their quantisation. Codes and scales bit-exact against the oracle fed
+    the GPU's permutation; the forward within the acceptance bound, and against the oracle on its plan."""
+    cfg = synth.custom(S, D=D, H=2, k=max(1, S // 128), iters=2)
+    Q, K, V = synth.make_inputs(cfg, seed=31, device="cuda")
+    flags = m.VC_VSMOOTH | m.VC_QK_HADAMARD | (m.VC_KCENTER if kcenter else 0)
+    plan = m.vc_attn_prepare_ex(Q, K, V, cfg["k"], cfg["iters"], flags=flags)
+    O = m.vc_attn_forward(plan)
+    assert m.vc_plan_status(plan) == (0, 0)
+    allp = gpu_plan_all(m, plan)
+    rows = np.arange(S)
+    fl = oracle.EXPCAST | oracle.MIDWINDOW | oracle.HADAMARD
+    for h in range(2):
+        g = head_of(allp, 0, h)
+        o = oracle.prepare_head(u16(Q[0, h]), u16(K[0, h]), u16(V[0, h]), cfg["k"], cfg["iters"], perm=g["perm"],
+                                kcenter=kcenter, hadamard=True)
+        compare_prep(g, o, S)
+        ref, _, _ = oracle.forward_head(o, rows)
+        got = f64(O[0, h])
+        assert_within(got, ref, float(np.abs(f64(V[0, h])).max()), f"head {h}")
+        fwd = oracle.attention_quant(g["qc"], g["sq"], g["kc"], g["sk"], g["rc"], g["sv"], g["mub"], S, rows, fl)[0]
+        rel_f, _ = errors(got, fwd)
+        assert rel_f <= FWD_ONLY_REL, f"head {h}: forward-only rel-L2 {rel_f:.3e}"
+    plan.destroy()

@@ -47,11 +47,12 @@ def plan_repair(m, plan):
     (300, 64, 300, 0),                 # every token repaired
     (1, 64, 1, 0),                     # one token: one key tile and one repair tile
     (129, 128, 129, "channel"),        # two ragged key tiles, two repair tiles, every token repaired
+    (1000, 64, 50, "hadamard"),        # rotated Q and K, the copied keys rotated alike
 ])
 def test_repair_parity(m, S, D, n, flags):
     H = 2
     Q, K, V = heavy_inputs(S, D, H, seed=S + n)
-    f = {"kcenter": m.VC_KCENTER, "channel": m.VC_VSCALE_CHANNEL}.get(flags, 0)
+    f = {"kcenter": m.VC_KCENTER, "channel": m.VC_VSCALE_CHANNEL, "hadamard": m.VC_QK_HADAMARD}.get(flags, 0)
     plan = m.vc_attn_prepare_repair(Q, K, V, n, flags=f)
     assert plan.n_repair == n
     O = m.vc_attn_forward(plan, flags=m.VC_EXPCAST | m.VC_MIDWINDOW)
@@ -63,7 +64,8 @@ def test_repair_parity(m, S, D, n, flags):
     for h in range(H):
         g = head_of(allp, 0, h)
         o = oracle.prepare_head(u16(Q[0, h]), u16(K[0, h]), u16(V[0, h]), 1, 1, vsmooth=False,
-                                kcenter=flags == "kcenter", vscale_channel=flags == "channel", n_repair=n)
+                                kcenter=flags == "kcenter", vscale_channel=flags == "channel", n_repair=n,
+                                hadamard=flags == "hadamard")
         if flags == "channel":
             assert np.array_equal(svc[0, h], o["sv"])
             assert np.array_equal(g["rc"], o["rc"]) and np.array_equal(g["qc"], o["qc"])
@@ -79,7 +81,8 @@ def test_repair_parity(m, S, D, n, flags):
         got = f64(O[0, h])
         assert_within(got, ref, float(np.abs(f64(V[0, h])).max()), f"head {h}")
         sv = svc[0, h] if flags == "channel" else g["sv"]
-        fwd = oracle.attention_quant(g["qc"], g["sq"], g["kc"], g["sk"], g["rc"], sv, None, S, rows,
+        fl = oracle.EXPCAST | oracle.MIDWINDOW | (oracle.HADAMARD if flags == "hadamard" else 0)
+        fwd = oracle.attention_quant(g["qc"], g["sq"], g["kc"], g["sk"], g["rc"], sv, None, S, rows, fl,
                                      repair={"n": n, "kc": rp["kc"][0, h], "sk": rp["sk"][0, h],
                                              "rc": rp["vt"][0, h].T})[0]
         rel_f, _ = errors(got, fwd)
