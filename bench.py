@@ -437,7 +437,8 @@ def main():
         "roofline": {"bound": "tensor", "kernel": forward_kernel_name(cfg["D"]), "achieved": fwd_tflops,
                      "peak": fp8_peak,
                      "unit": "TFLOP/s", "frac": fwd_tflops / fp8_peak, "traffic": profiled_traffic(cfg),
-                     "peak_source": f"{src} bf16 burst {bf16_burst:.0f} TFLOP/s x {FP8_OVER_BF16:.0f} (FP8/BF16 nominal)"},
+                     "peak_source": f"{src} bf16 burst {bf16_burst:.0f} TFLOP/s x {FP8_OVER_BF16:.0f} "
+                                    "(FP8/BF16 nominal)"},
         "clocks": clocks, "gpu_launches": launches_per_step(cfg) * args.steps,
     }
     if e2e:

@@ -60,7 +60,8 @@ VC_NOALLOC_MAX_HEADS = 4096
 VC_STEP_GROUP, VC_STEP_GROUP_WARM, VC_STEP_REUSE, VC_STEP_PLAIN = 0, 1, 2, 3
 
 EXPORTS = ("vc_attn_prepare", "vc_attn_prepare_ex", "vc_attn_prepare_repair", "vc_attn_forward", "vc_plan_size",
-           "vc_plan_get", "vc_plan_status", "vc_plan_shape", "vc_plan_destroy", "vc_expcast_encode", "vc_schedule_action",
+           "vc_plan_get", "vc_plan_status", "vc_plan_shape", "vc_plan_destroy", "vc_expcast_encode",
+           "vc_schedule_action",
            "vc_strerror", "vc_version")
 
 

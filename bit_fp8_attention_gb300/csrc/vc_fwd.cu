@@ -12,7 +12,8 @@
 //   producer    TMA: Q once; K' and V^T tiles of 128 keys into 3-stage rings; with
 //               V-Smooth, the transposed bf16 means of each 16-tile block run into a 2-stage ring.
 //   MMA issuer  one warp, one elected lane issuing: S = Q K'^T for two key tiles at once
-//               (kind::f8f6f4, SS, N = 256) into the two TMEM score buffers; O += P V and W += P E_{j mod 16} (TS: the codes P are read from TMEM),
+//               (kind::f8f6f4, SS, N = 256) into the two TMEM score buffers; O += P V and
+//               W += P E_{j mod 16} (TS: the codes P are read from TMEM),
 //               where E_s is a one-hot 16 x 128 block, so column j mod 16 of W receives the exact
 //               row sum of tile j; at the end of each run of tiles from one 16-tile block, the
 //               mean term O += F M^T (kind::f16, F = W / sV split into bf16 hi + lo, M the block's
@@ -473,7 +474,9 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
       const float mx = fmaxf(max3f(m8[0], m8[1], m8[2]), max3f(max3f(m8[3], m8[4], m8[5]), m8[6], m8[7]));
       const float aj = aq * sk;
       const float tmax = mx * aj;  // = max_c fl(s_c * a_j): rounding is monotone and a_j > 0
-      if (t + 1 < ntiles) {  // (with repair tiles the last regular tile's max goes over too)  // the tile max goes to the other group at once; it depends on nothing else
+      // The tile max goes to the other group at once; it depends on nothing else (with repair tiles the
+      // last regular tile's max goes over too).
+      if (t + 1 < ntiles) {
         mbuf[(t & 7) * 128 + row] = tmax;
         mbar_arrive(&mx_full[(t & 7) * 4 + wq]);  // release: orders this lane's store before the arrival
       }

@@ -420,7 +420,8 @@ __global__ void __launch_bounds__(352, 1) vc_fwd2_kernel(const __grid_constant__
       if constexpr (kExpCast) {
         if (__all_sync(0xffffffffu, fabsf(Mn) < kClampFreeMaxAbsM)) {
 #pragma unroll
-          for (int q = 0; q < 32; ++q) pk[q] = expcast4(s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3], a2, a2, b2, b2);
+          for (int q = 0; q < 32; ++q)
+            pk[q] = expcast4(s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3], a2, a2, b2, b2);
         } else {  // a running max beyond 2^22 code units: clip the codes at 120 byte by byte
 #pragma unroll
           for (int q = 0; q < 32; ++q)
@@ -594,8 +595,10 @@ int forward2_launch(const PlanBuffers& p, const FwdMaps& maps, uint16_t* O, unsi
   if (p.D != 64) return VC_ERR_UNSUPPORTED;
   const bool ec = (flags & VC_EXPCAST) != 0;
   if (p.nrt > 0)
-    return ec ? launch_fwd2<64, true, true>(p, maps, O, flags, st) : launch_fwd2<64, false, true>(p, maps, O, flags, st);
-  return ec ? launch_fwd2<64, true, false>(p, maps, O, flags, st) : launch_fwd2<64, false, false>(p, maps, O, flags, st);
+    return ec ? launch_fwd2<64, true, true>(p, maps, O, flags, st)
+              : launch_fwd2<64, false, true>(p, maps, O, flags, st);
+  return ec ? launch_fwd2<64, true, false>(p, maps, O, flags, st)
+            : launch_fwd2<64, false, false>(p, maps, O, flags, st);
 }
 
 }  // namespace vc

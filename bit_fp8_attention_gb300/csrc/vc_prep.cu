@@ -227,12 +227,13 @@ void quant_blocks_launch(const uint16_t* x, const int32_t* perm, const uint16_t*
                          int S_src, int BH, uint8_t* codes, float* scales, cudaStream_t st, bool rotate) {
   const dim3 grid(S_pad / 128, BH);
   if (rotate) {
+    const uint16_t* c = center;
     if (D == 128) {
-      if (center) quant_blocks_rot_kernel<128, true><<<grid, 256, 0, st>>>(x, perm, center, S, S_pad, S_src, codes, scales);
-      else quant_blocks_rot_kernel<128, false><<<grid, 256, 0, st>>>(x, perm, nullptr, S, S_pad, S_src, codes, scales);
+      if (c) quant_blocks_rot_kernel<128, true><<<grid, 256, 0, st>>>(x, perm, c, S, S_pad, S_src, codes, scales);
+      else quant_blocks_rot_kernel<128, false><<<grid, 256, 0, st>>>(x, perm, c, S, S_pad, S_src, codes, scales);
     } else {
-      if (center) quant_blocks_rot_kernel<64, true><<<grid, 256, 0, st>>>(x, perm, center, S, S_pad, S_src, codes, scales);
-      else quant_blocks_rot_kernel<64, false><<<grid, 256, 0, st>>>(x, perm, nullptr, S, S_pad, S_src, codes, scales);
+      if (c) quant_blocks_rot_kernel<64, true><<<grid, 256, 0, st>>>(x, perm, c, S, S_pad, S_src, codes, scales);
+      else quant_blocks_rot_kernel<64, false><<<grid, 256, 0, st>>>(x, perm, c, S, S_pad, S_src, codes, scales);
     }
     return;
   }

@@ -113,7 +113,8 @@ typedef struct vc_plan vc_plan;
  *   mu_j = mean of the valid rows of block j of V', stored as bf16; R = V' - mu_j quantised to
  *   E4M3 with one scale per head (absmax/448), stored transposed and padded.
  * Q, K, V: device bf16 [B, H, S, D].  k_clusters, iters: k-means size and rounds
- * (1 <= iters <= 64, else VC_ERR_INVALID_ARG; each round = assignment, argsort, centroid update).  *plan: NULL to allocate a new plan, or an
+ * (1 <= iters <= 64, else VC_ERR_INVALID_ARG; each round = assignment, argsort, centroid update).
+ * *plan: NULL to allocate a new plan, or an
  * existing plan of the same (B, H, S, D, k_clusters), whose buffers are reused without any
  * allocation (VC_ERR_PLAN_MISMATCH if the shape differs; the plan is left untouched).
  * The first call allocates device memory (synchronous cudaMalloc); later calls reusing the plan
