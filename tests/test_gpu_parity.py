@@ -100,6 +100,13 @@ def test_ragged_shapes(m, S, D):
     check_config(m, cfg)
 
 
+@pytest.mark.parametrize("S,D", [(300, 64), (257, 128)])
+def test_batch_dimension(m, S, D):
+    """B > 1: every (b, h) pair is its own head in the plan and in the output."""
+    cfg = synth.custom(S, D=D, H=3, B=2, k=3, iters=2)
+    check_config(m, cfg)
+
+
 @pytest.mark.parametrize("expcast,midwindow,vsmooth", [(False, True, True), (True, False, True),
                                                        (True, True, False), (False, False, False)])
 def test_ablations(m, expcast, midwindow, vsmooth):

@@ -21,8 +21,8 @@ def m():
     return vc()
 
 
-def heavy_inputs(S, D, H, seed):
-    cfg = synth.custom(S, D=D, H=H, k=max(1, S // 128), iters=1)
+def heavy_inputs(S, D, H, seed, B=1):
+    cfg = synth.custom(S, D=D, H=H, B=B, k=max(1, S // 128), iters=1)
     Q, K, V = synth.make_inputs(cfg, seed=seed, device="cuda")
     gen = torch.Generator().manual_seed(seed + 1)
     gain = torch.ones(S)
@@ -48,10 +48,12 @@ def plan_repair(m, plan):
     (1, 64, 1, 0),                     # one token: one key tile and one repair tile
     (129, 128, 129, "channel"),        # two ragged key tiles, two repair tiles, every token repaired
     (1000, 64, 50, "hadamard"),        # rotated Q and K, the copied keys rotated alike
+    (700, 128, 20, "batch"),           # B = 2: each batch-head selects its own tokens
+    (500, 64, 9, "batch"),
 ])
 def test_repair_parity(m, S, D, n, flags):
-    H = 2
-    Q, K, V = heavy_inputs(S, D, H, seed=S + n)
+    H, B = 2, 2 if flags == "batch" else 1
+    Q, K, V = heavy_inputs(S, D, H, seed=S + n, B=B)
     f = {"kcenter": m.VC_KCENTER, "channel": m.VC_VSCALE_CHANNEL, "hadamard": m.VC_QK_HADAMARD}.get(flags, 0)
     plan = m.vc_attn_prepare_repair(Q, K, V, n, flags=f)
     assert plan.n_repair == n
@@ -61,30 +63,30 @@ def test_repair_parity(m, S, D, n, flags):
     rp = plan_repair(m, plan)
     svc = m.vc_plan_get(plan, m.VC_PLAN_VCHSCALES).cpu().numpy()
     rows = np.arange(S)
-    for h in range(H):
-        g = head_of(allp, 0, h)
-        o = oracle.prepare_head(u16(Q[0, h]), u16(K[0, h]), u16(V[0, h]), 1, 1, vsmooth=False,
+    for b, h in ((b, h) for b in range(B) for h in range(H)):
+        g = head_of(allp, b, h)
+        o = oracle.prepare_head(u16(Q[b, h]), u16(K[b, h]), u16(V[b, h]), 1, 1, vsmooth=False,
                                 kcenter=flags == "kcenter", vscale_channel=flags == "channel", n_repair=n,
                                 hadamard=flags == "hadamard")
         if flags == "channel":
-            assert np.array_equal(svc[0, h], o["sv"])
+            assert np.array_equal(svc[b, h], o["sv"])
             assert np.array_equal(g["rc"], o["rc"]) and np.array_equal(g["qc"], o["qc"])
         else:
             compare_prep(g, o, S)
         orp = o["repair"]
-        assert np.array_equal(rp["energy"][0, h], orp["energy"]), f"head {h}: energies"
-        assert np.array_equal(rp["idx"][0, h], orp["idx"]), f"head {h}: selected tokens"
-        assert np.array_equal(rp["kc"][0, h], orp["kc"]), f"head {h}: copied key codes"
-        assert np.array_equal(rp["sk"][0, h], orp["sk"]), f"head {h}: copied key scales"
-        assert np.array_equal(rp["vt"][0, h].T, orp["rc"]), f"head {h}: repair residual codes"
+        assert np.array_equal(rp["energy"][b, h], orp["energy"]), f"head {h}: energies"
+        assert np.array_equal(rp["idx"][b, h], orp["idx"]), f"head {h}: selected tokens"
+        assert np.array_equal(rp["kc"][b, h], orp["kc"]), f"head {h}: copied key codes"
+        assert np.array_equal(rp["sk"][b, h], orp["sk"]), f"head {h}: copied key scales"
+        assert np.array_equal(rp["vt"][b, h].T, orp["rc"]), f"head {h}: repair residual codes"
         ref, _, _ = oracle.forward_head(o, rows)
-        got = f64(O[0, h])
-        assert_within(got, ref, float(np.abs(f64(V[0, h])).max()), f"head {h}")
-        sv = svc[0, h] if flags == "channel" else g["sv"]
+        got = f64(O[b, h])
+        assert_within(got, ref, float(np.abs(f64(V[b, h])).max()), f"head {h}")
+        sv = svc[b, h] if flags == "channel" else g["sv"]
         fl = oracle.EXPCAST | oracle.MIDWINDOW | (oracle.HADAMARD if flags == "hadamard" else 0)
         fwd = oracle.attention_quant(g["qc"], g["sq"], g["kc"], g["sk"], g["rc"], sv, None, S, rows, fl,
-                                     repair={"n": n, "kc": rp["kc"][0, h], "sk": rp["sk"][0, h],
-                                             "rc": rp["vt"][0, h].T})[0]
+                                     repair={"n": n, "kc": rp["kc"][b, h], "sk": rp["sk"][b, h],
+                                             "rc": rp["vt"][b, h].T})[0]
         rel_f, _ = errors(got, fwd)
         assert rel_f <= FWD_ONLY_REL, f"head {h}: forward-only rel-L2 {rel_f:.3e}"
     plan.destroy()
