@@ -132,44 +132,52 @@ __global__ void __launch_bounds__(256) quant_blocks_kernel(const uint16_t* __res
 // The same quantiser with each row rotated first ("VC-Attention", Sec. 3.4 "Fused preprocessing", App. B:
 // the Q and K passes fuse a Hadamard rotation): the unnormalised Walsh-Hadamard transform in fp32, as
 // the butterfly with stages s = 1, 2, ..., D/2 in that order, pair (x[i], x[i+s]) -> (x[i] + x[i+s],
-// x[i] - x[i+s]). A thread holds 8 consecutive channels of a row, so stages 1-4 stay in its registers
-// and stages 8 and up pair it with the lane holding the partner chunk (lane ^ s/8, same row).
+// x[i] - x[i+s]). A thread holds 32 consecutive channels of a row, so stages 1-16 stay in its registers
+// and stages 32 and up pair it with the lane holding the partner channels (lane ^ s/32, same row).
 template <int D, bool kCentred>
 __global__ void __launch_bounds__(256) quant_blocks_rot_kernel(const uint16_t* __restrict__ x,
                                                                const int32_t* __restrict__ perm,
                                                                const uint16_t* __restrict__ center, int S,
                                                                int S_pad, int S_src, uint8_t* __restrict__ codes,
                                                                float* __restrict__ scales) {
-  constexpr int CPR = D / 8;                 // 16-byte chunks per row
-  constexpr int NCH = 128 * CPR / 256;       // chunks per thread
-  static_assert(32 % CPR == 0, "a row's chunks sit in consecutive lanes of one warp");
+  constexpr int G = 4;                       // 16-byte chunks per thread and row: 32 channels
+  constexpr int W = 8 * G;
+  constexpr int TPR = D / W;                 // threads per row
+  constexpr int RSTEP = 256 / TPR;           // rows between a thread's rows
+  constexpr int RPT = 128 / RSTEP;           // rows per thread
+  static_assert(32 % TPR == 0 && RPT >= 1, "a row's threads sit in consecutive lanes of one warp");
   const int j = blockIdx.x, bh = blockIdx.y;
   const int nkb = S_pad / 128;
   const uint16_t* xh = x + (int64_t)bh * S_src * D;
   const int32_t* ph = perm ? perm + (int64_t)bh * S : nullptr;
-  const int cc = threadIdx.x % CPR;          // this thread's chunk of every row it holds
-  __shared__ uint4 cen_s[CPR];
+  const int sub = threadIdx.x % TPR;         // channels [W sub, W sub + W) of rows r0 + RSTEP m
+  const int r0 = threadIdx.x / TPR;
+  __shared__ uint4 cen_s[D / 8];
   __shared__ float red[8];
-  if (kCentred && threadIdx.x < CPR)
+  if (kCentred && threadIdx.x < D / 8)
     cen_s[threadIdx.x] = __ldg(reinterpret_cast<const uint4*>(center + (int64_t)bh * D) + threadIdx.x);
-  uint4 v[NCH];
+  uint4 v[RPT][G];
 #pragma unroll
-  for (int m = 0; m < NCH; ++m) {
-    const int t = j * 128 + (threadIdx.x + 256 * m) / CPR;
-    v[m] = make_uint4(0, 0, 0, 0);
-    if (t < S) v[m] = *reinterpret_cast<const uint4*>(xh + (int64_t)(ph ? ph[t] : t) * D + cc * 8);
+  for (int m = 0; m < RPT; ++m) {
+    const int t = j * 128 + r0 + RSTEP * m;
+    const uint4* src = t < S ? reinterpret_cast<const uint4*>(xh + (int64_t)(ph ? ph[t] : t) * D + sub * W) : nullptr;
+#pragma unroll
+    for (int g = 0; g < G; ++g) v[m][g] = src ? src[g] : make_uint4(0, 0, 0, 0);
   }
   if (kCentred) __syncthreads();
-  const uint4 cm = kCentred ? cen_s[cc] : make_uint4(0, 0, 0, 0);
-  float y[NCH][8];
+  float y[RPT][W];
 #pragma unroll
-  for (int m = 0; m < NCH; ++m) {
+  for (int m = 0; m < RPT; ++m) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) y[m][i] = chunk_elem<kCentred>(v[m], cm, i);
+    for (int g = 0; g < G; ++g) {
+      const uint4 cm = kCentred ? cen_s[sub * G + g] : make_uint4(0, 0, 0, 0);
 #pragma unroll
-    for (int s = 1; s < 8; s <<= 1)
+      for (int i = 0; i < 8; ++i) y[m][8 * g + i] = chunk_elem<kCentred>(v[m][g], cm, i);
+    }
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+    for (int s = 1; s < W; s <<= 1)
+#pragma unroll
+      for (int i = 0; i < W; ++i)
         if (!(i & s)) {
           const float a = y[m][i], b = y[m][i + s];
           y[m][i] = __fadd_rn(a, b);
@@ -177,24 +185,24 @@ __global__ void __launch_bounds__(256) quant_blocks_rot_kernel(const uint16_t* _
         }
   }
 #pragma unroll
-  for (int s = 8; s < D; s <<= 1) {
-    const int lm = s / 8;                     // partner lane offset
-    const bool lower = (cc & lm) == 0;        // this chunk holds x[i], the partner x[i + s]
+  for (int s = W; s < D; s <<= 1) {
+    const int lm = s / W;                     // partner lane offset
+    const bool lower = (sub & lm) == 0;       // this thread holds x[i], the partner x[i + s]
 #pragma unroll
-    for (int m = 0; m < NCH; ++m)
+    for (int m = 0; m < RPT; ++m)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < W; ++i) {
         const float p = __shfl_xor_sync(0xffffffffu, y[m][i], lm);
         y[m][i] = lower ? __fadd_rn(y[m][i], p) : __fsub_rn(p, y[m][i]);
       }
   }
   float amax = 0.f;
 #pragma unroll
-  for (int m = 0; m < NCH; ++m) {
+  for (int m = 0; m < RPT; ++m) {
     float a = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(y[m][i]));
-    if (j * 128 + (threadIdx.x + 256 * m) / CPR < S) amax = fmaxf(amax, a);  // pad rows do not count
+    for (int i = 0; i < W; ++i) a = fmaxf(a, fabsf(y[m][i]));
+    if (j * 128 + r0 + RSTEP * m < S) amax = fmaxf(amax, a);  // pad rows do not count
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -208,17 +216,19 @@ __global__ void __launch_bounds__(256) quant_blocks_rot_kernel(const uint16_t* _
   if (threadIdx.x == 0) scales[(int64_t)bh * nkb + j] = zero ? 1.f : __fdiv_rn(amax, 448.f);
   uint8_t* ch = codes + ((int64_t)bh * S_pad + (int64_t)j * 128) * D;
 #pragma unroll
-  for (int m = 0; m < NCH; ++m) {
-    const int r = (threadIdx.x + 256 * m) / CPR;
-    uint32_t lo = 0, hi = 0;
-    if (!zero && j * 128 + r < S) {
-      uint32_t w[4];
+  for (int m = 0; m < RPT; ++m) {
+    const int r = r0 + RSTEP * m;
+    const bool live = !zero && j * 128 + r < S;
+    uint32_t w[W / 4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) w[q] = cvt_e4m3x2(__fmul_rn(y[m][2 * q], inv), __fmul_rn(y[m][2 * q + 1], inv));
-      lo = w[0] | (w[1] << 16);
-      hi = w[2] | (w[3] << 16);
+    for (int q = 0; q < W / 4; ++q) {
+      const uint32_t lo = cvt_e4m3x2(__fmul_rn(y[m][4 * q], inv), __fmul_rn(y[m][4 * q + 1], inv));
+      const uint32_t hi = cvt_e4m3x2(__fmul_rn(y[m][4 * q + 2], inv), __fmul_rn(y[m][4 * q + 3], inv));
+      w[q] = live ? (lo | (hi << 16)) : 0u;
     }
-    *reinterpret_cast<uint2*>(ch + (int64_t)r * D + cc * 8) = make_uint2(lo, hi);
+    uint4* dst = reinterpret_cast<uint4*>(ch + (int64_t)r * D + sub * W);
+#pragma unroll
+    for (int q = 0; q < W / 16; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
   }
 }
 
@@ -316,7 +326,8 @@ __global__ void iota_kernel(int32_t* __restrict__ perm, int S, int64_t total) {
 
 // ---------------------------------------------------------------------------------------------
 // Block means of V' = V[pi] and the per-head residual maximum.  One CTA per (block, bh); the block's
-// rows are gathered into shared memory once.
+// rows are gathered into shared memory once, and each thread then holds one channel pair of
+// 128/PARTS rows in registers for all three passes (largest exponent, exact sum, residual maximum).
 // mu_j = (sum of the valid rows) / n_j, rounded once to bf16. The sum is exact: every bf16 value is an
 // 8-bit significand M times 2^(E-134); relative to the column's largest exponent E_max it becomes the
 // integer M * 2^(E - E_max + 45) (|sum| < 2^60 in int64), exact whenever the column spans at most 45
@@ -324,77 +335,104 @@ __global__ void iota_kernel(int32_t* __restrict__ perm, int S, int64_t total) {
 // (sum * 2^(E_max - 179)) / n_j is then the same double, and so is the bf16 mean. R = V' - mu_b in
 // fp32; amax_h = max |R| over the head (atomicMax on the bit pattern of a non-negative float) and,
 // when amax_ch is given, amax_d = max |R[:, d]| of every channel over the head the same way.
+__device__ __forceinline__ long long exact_term(uint32_t b, int em) {
+  const int e = (b >> 7) & 0xFF;
+  const long long m = (long long)((b & 0x7Fu) | (e ? 0x80u : 0u));
+  const int sh = max(e, 1) - em + 45;  // in [.., 45]; below 0 only past a 45-binade span
+  const long long x = sh >= 0 ? (m << sh) : (m >> min(-sh, 63));
+  return (b & 0x8000u) ? -x : x;
+}
+
 template <int D>
 __global__ void __launch_bounds__(256) vmeans_kernel(const uint16_t* __restrict__ v, const int32_t* __restrict__ perm,
                                                      int S, int demean, uint16_t* __restrict__ mub,
                                                      unsigned int* __restrict__ amax_bits,
                                                      uint16_t* __restrict__ mubT = nullptr, int nkb16 = 0,
                                                      unsigned int* __restrict__ amax_ch = nullptr) {
-  constexpr int SPLIT = 256 / D;  // threads per column
+  constexpr int NP = D / 2;          // channel pairs
+  constexpr int PARTS = 256 / NP;    // threads per pair
+  constexpr int RPT = 128 / PARTS;   // rows per thread: part, part + PARTS, ...
   const int j = blockIdx.x, bh = blockIdx.y;
   const int nkb = (S + 127) / 128;
-  const int d = threadIdx.x % D, part = threadIdx.x / D;
+  const int c = threadIdx.x % NP, part = threadIdx.x / NP;
   const int t0 = j * 128, n = min(128, S - t0);
   const uint16_t* vh = v + (int64_t)bh * S * D;
   const int32_t* ph = perm ? perm + (int64_t)bh * S : nullptr;
   __shared__ __align__(16) uint16_t blk[128][D];
-  __shared__ int emax_part[SPLIT][D];
-  __shared__ long long sums[SPLIT][D];
+  __shared__ uint32_t emax_part[PARTS][NP];
+  __shared__ long long sums[PARTS][D];
+  __shared__ int emc[D];
   __shared__ float mus[D];
   __shared__ float red[8];
-  __shared__ float cmax[SPLIT][D];
-  gather_block<D>(blk, vh, ph, t0, n);
+  __shared__ float cmax[PARTS][D];
+  gather_block<D>(blk, vh, ph, t0, n);  // rows n..127 read as +0: no exponent, no sum term
   __syncthreads();
-  // exponent field with subnormals and zero read as 1, as in M * 2^(E - 134)
-  int em = 1;
-  for (int r = part; r < n; r += SPLIT) em = max(em, max((blk[r][d] >> 7) & 0xFF, 1));
-  emax_part[part][d] = em;
+  uint32_t w[RPT];  // (channel 2c) | (channel 2c + 1) << 16 of row part + PARTS * i
+  const uint32_t* bw = reinterpret_cast<const uint32_t*>(&blk[0][0]);
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) w[i] = bw[(part + PARTS * i) * NP + c];
+  // exponent fields of both channels in place, with subnormals and zero read as 1 below
+  uint32_t ex = 0;
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) ex = __vmaxu2(ex, w[i] & 0x7F807F80u);
+  emax_part[part][c] = ex;
   __syncthreads();
 #pragma unroll
-  for (int q = 0; q < SPLIT; ++q) em = max(em, emax_part[q][d]);
-  long long acc = 0;
-  for (int r = part; r < n; r += SPLIT) {
-    const uint32_t b = blk[r][d];
-    const int e = (b >> 7) & 0xFF;
-    const long long m = (long long)((b & 0x7Fu) | (e ? 0x80u : 0u));
-    const int sh = max(e, 1) - em + 45;  // in [.., 45]; below 0 only past a 45-binade span
-    const long long x = sh >= 0 ? (m << sh) : (m >> min(-sh, 63));
-    acc += (b & 0x8000u) ? -x : x;
+  for (int q = 0; q < PARTS; ++q) ex = __vmaxu2(ex, emax_part[q][c]);
+  const int em0 = max((int)((ex >> 7) & 0xFFu), 1), em1 = max((int)((ex >> 23) & 0xFFu), 1);
+  long long a0 = 0, a1 = 0;
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    a0 += exact_term(w[i] & 0xFFFFu, em0);
+    a1 += exact_term(w[i] >> 16, em1);
   }
-  sums[part][d] = acc;
-  __syncthreads();
+  sums[part][2 * c] = a0;
+  sums[part][2 * c + 1] = a1;
   if (part == 0) {
+    emc[2 * c] = em0;
+    emc[2 * c + 1] = em1;
+  }
+  __syncthreads();
+  if (threadIdx.x < D) {
+    const int d = threadIdx.x;
     long long tot = 0;
 #pragma unroll
-    for (int q = 0; q < SPLIT; ++q) tot += sums[q][d];
-    const double total = ldexp((double)tot, em - 179);  // 2^(E - 134) * 2^-45
+    for (int q = 0; q < PARTS; ++q) tot += sums[q][d];
+    const double total = ldexp((double)tot, emc[d] - 179);  // 2^(E - 134) * 2^-45
     uint16_t b = demean ? f64_to_bf16_rne(total / (double)n) : (uint16_t)0;
     mub[((int64_t)bh * nkb + j) * D + d] = b;
     if (mubT) mubT[((int64_t)bh * D + d) * nkb16 + j] = b;  // [BH, D, nkb16]: the forward's flush operand
     mus[d] = bf16_bits_to_f32(b);
   }
   __syncthreads();
-  float amax = 0.f;
-  for (int r = part; r < n; r += SPLIT) {
-    float res = __fsub_rn(bf16_bits_to_f32(blk[r][d]), mus[d]);
-    amax = fmaxf(amax, fabsf(res));
+  const float mu0 = mus[2 * c], mu1 = mus[2 * c + 1];
+  float am0 = 0.f, am1 = 0.f;
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    if (part + PARTS * i < n) {
+      am0 = fmaxf(am0, fabsf(__fsub_rn(bf16_bits_to_f32(w[i] & 0xFFFFu), mu0)));
+      am1 = fmaxf(am1, fabsf(__fsub_rn(__uint_as_float(w[i] & 0xFFFF0000u), mu1)));
+    }
   }
   if (amax_ch) {  // per channel: combine the column's parts, one atomic per channel
-    cmax[part][d] = amax;
+    cmax[part][2 * c] = am0;
+    cmax[part][2 * c + 1] = am1;
     __syncthreads();
-    if (part == 0) {
+    if (threadIdx.x < D) {
+      const int d = threadIdx.x;
       float m = cmax[0][d];
 #pragma unroll
-      for (int q = 1; q < SPLIT; ++q) m = fmaxf(m, cmax[q][d]);
+      for (int q = 1; q < PARTS; ++q) m = fmaxf(m, cmax[q][d]);
       atomicMax(amax_ch + (int64_t)bh * D + d, __float_as_uint(m));
     }
   }
+  float amax = fmaxf(am0, am1);
   for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
   __syncthreads();
   if (threadIdx.x == 0) {
     float m = red[0];
-    for (int w = 1; w < 8; ++w) m = fmaxf(m, red[w]);
+    for (int w8 = 1; w8 < 8; ++w8) m = fmaxf(m, red[w8]);
     atomicMax(amax_bits + bh, __float_as_uint(m));
   }
 }
