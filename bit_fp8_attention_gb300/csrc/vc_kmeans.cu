@@ -6,11 +6,13 @@
 // index on a tie; a centroid becomes the mean of its members, an empty cluster keeps its centroid.
 //
 // GB300 design:
-//   assignment  tcgen05 (kind::f16): per CTA two 128-token tiles of V (bf16, exact) against the
-//               centroids in chunks of 128, each centroid split into bf16 hi + lo (about 16
-//               significant bits); fp32 dot products accumulate in TMEM (two tiles x two chunk
-//               buffers = 512 columns), eight epilogue warps scan the columns in ascending order
-//               for argmin ||c||^2 - 2 x.c. One warp loads by TMA, one thread issues the MMAs.
+//   assignment  tcgen05 (kind::f16), persistent (one CTA per SM): per work item two 128-token
+//               tiles of V (bf16, exact) against the centroids in chunks of 64, each centroid split
+//               into bf16 hi + lo (about 16 significant bits); fp32 dot products accumulate in TMEM
+//               (two tiles x two chunk buffers = 256 columns), eight epilogue warps scan the columns
+//               in ascending order for argmin ||c||^2 - 2 x.c. One warp loads the token tiles by TMA
+//               (double-buffered, so the next item's tiles land while this one computes), one the
+//               centroid chunks, and one elected thread issues the MMAs.
 //   argsort     stable counting sort in three launches: per-chunk label histograms, a scan over
 //               chunks and bins, then a scatter in token order within each chunk.
 //   update      one warp per cluster, compensated fp32 sums (TwoSum) of the member rows read
@@ -90,21 +92,22 @@ __global__ void __launch_bounds__(256) kmeans_init_kernel(const uint16_t* __rest
 // ---------------------------------------------------------------------------------------------
 template <int D>
 struct AsgCfg {
-  static constexpr int TPC = 2;                 // 128-token tiles per CTA
+  static constexpr int TPC = 2;                 // 128-token tiles per work item
   static constexpr int CH = 128;                // centroids per chunk (MMA N)
-  static constexpr int NST = 2;                 // chunk stages
+  static constexpr int NST = 3;                 // stages, each one part (hi or lo) of a chunk
+  static constexpr int NXB = 2;                 // token-tile buffers: the next item's tiles load during this one
   static constexpr int ATOM = 128 * 128;        // one 128-byte-swizzled K half of a 128-row operand
   static constexpr int HALVES = D / 64;         // K halves of 64 bf16
   static constexpr int XT = HALVES * ATOM;      // bytes of a token tile
-  static constexpr int CB = HALVES * ATOM;      // bytes of one part (hi or lo) of a chunk
+  static constexpr int CB = HALVES * CH * 128;  // bytes of one part (hi or lo) of a chunk
   static constexpr int OFF_X = 0;
-  static constexpr int OFF_C = OFF_X + TPC * XT;
-  static constexpr int OFF_BAR = OFF_C + NST * 2 * CB;
-  static constexpr int NBAR = 1 + 2 * NST + 2 + 2 + 1;
+  static constexpr int OFF_C = OFF_X + NXB * TPC * XT;
+  static constexpr int OFF_BAR = OFF_C + NST * CB;
+  static constexpr int NBAR = 2 * NXB + 2 * NST + 2 + 2 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int USED = OFF_MISC + 16 + 1024;  // + slack for aligning the base to 1024
-  // One CTA per SM: the kernel holds all 512 TMEM columns.
-  static constexpr int SMEM = USED > 120 * 1024 ? USED : 120 * 1024;
+  static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + slack for aligning the base to 1024
+  static constexpr int TMEM_COLS = TPC * 2 * CH;     // two accumulator buffers per tile
+  static_assert(SMEM <= 227 * 1024, "fits one SM's shared memory");
 };
 
 __device__ __forceinline__ void mma_bf16_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -128,19 +131,26 @@ __device__ __forceinline__ void fail(int* status, volatile int* abort_flag) {
 }
 
 // xmap: V as [B*H*S rows, D] bf16, box 64 x 128, 128-byte swizzle.
-// cmap: centroid splits as [B*H*2*kpad rows, D] bf16 (per head: kpad hi rows, then kpad lo rows).
+// cmap: centroid splits as [B*H*2*kpad rows, D] bf16 (per head: kpad hi rows, then kpad lo rows),
+//       box 64 x CH.
+// Persistent: CTA b takes work items b, b + gridDim.x, ... (item w = head w / ntp, tokens
+// [256 (w % ntp), 256 (w % ntp) + 256)), so that one item's token tiles load while the previous item
+// computes. Local item i uses token buffer i % 2; the c-th chunk this CTA consumes, counted over all
+// its items, uses accumulator buffer c % 2, and its parts (hi, lo) are the stage loads u = 2c, 2c + 1
+// (stage u % NST).
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     kmeans_assign_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap cmap,
-                         const float* __restrict__ cnormp, int S, int kpad, int32_t* __restrict__ labels,
-                         int* __restrict__ status) {
+                         const float* __restrict__ cnormp, int S, int kpad, int nwork,
+                         int32_t* __restrict__ labels, int* __restrict__ status) {
   using C = AsgCfg<D>;
   extern __shared__ uint8_t asg_smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(asg_smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sX = base + C::OFF_X;
   uint8_t* sC = base + C::OFF_C;
   uint64_t* x_full = reinterpret_cast<uint64_t*>(base + C::OFF_BAR);
-  uint64_t* c_full = x_full + 1;
+  uint64_t* x_empty = x_full + C::NXB;
+  uint64_t* c_full = x_empty + C::NXB;
   uint64_t* c_empty = c_full + C::NST;
   uint64_t* acc_full = c_empty + C::NST;  // per TMEM buffer: both tiles' dot products of a chunk
   uint64_t* acc_empty = acc_full + 2;     // per TMEM buffer: read by all eight epilogue warps
@@ -149,50 +159,73 @@ __global__ void __launch_bounds__(320, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base + C::OFF_MISC + 8);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.y;
-  const int t0 = blockIdx.x * C::TPC * 128;
+  const int ntp = (S + C::TPC * 128 - 1) / (C::TPC * 128);  // work items per head
   const int nch = kpad / C::CH;
+  const int nitems = nwork > (int)blockIdx.x ? (nwork - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
 
   if (tid == 0) {
-    mbar_init(x_full, 1);
+    for (int x = 0; x < C::NXB; ++x) { mbar_init(&x_full[x], 1); mbar_init(&x_empty[x], 1); }
     for (int s = 0; s < C::NST; ++s) { mbar_init(&c_full[s], 1); mbar_init(&c_empty[s], 1); }
     for (int b = 0; b < 2; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 256); }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0) tmem_alloc(tmem_slot, 512);
+  if (warp == 0) tmem_alloc(tmem_slot, C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
-    // ---------------------------------------------------------------- TMA producer
+  if (warp == 10) {
+    // ---------------------------------------------------------------- TMA producer: token tiles
     if (lane == 0) {
       prefetch_tmap(&xmap);
+      int issued = 0;
+      for (int i = 0; i < nitems; ++i) {
+        const int xb = i % C::NXB;
+        if (i >= C::NXB && !wait_or_abort(&x_empty[xb], ((i / C::NXB) & 1) ^ 1, abort_flag)) {
+          fail(status, abort_flag);
+          break;
+        }
+        const int w = blockIdx.x + i * gridDim.x;
+        const int bh = w / ntp, t0 = (w % ntp) * C::TPC * 128;
+        mbar_arrive_expect_tx(&x_full[xb], C::TPC * C::XT);
+        for (int g = 0; g < C::TPC; ++g)
+          for (int h = 0; h < C::HALVES; ++h)
+            tma_load_2d(sX + (xb * C::TPC + g) * C::XT + h * C::ATOM, &xmap, h * 64, bh * S + t0 + g * 128,
+                        &x_full[xb]);
+        issued = i + 1;
+      }
+      // Teardown: every load issued into this CTA's shared memory has landed.
+      bool done = true;
+      for (int i = issued > C::NXB ? issued - C::NXB : 0; i < issued; ++i)
+        done &= mbar_wait(&x_full[i % C::NXB], (i / C::NXB) & 1, kWaitLimit);
+      if (!done) fail(status, abort_flag);
+    }
+  } else if (warp == 8) {
+    // ---------------------------------------------------------------- TMA producer: centroid chunks
+    if (lane == 0) {
       prefetch_tmap(&cmap);
-      mbar_arrive_expect_tx(x_full, C::TPC * C::XT);
-      for (int g = 0; g < C::TPC; ++g)
-        for (int h = 0; h < C::HALVES; ++h)
-          tma_load_2d(sX + g * C::XT + h * C::ATOM, &xmap, h * 64, bh * S + t0 + g * 128, x_full);
       int issued = 0;
       bool ok = true;
-      for (int ch = 0; ch < nch; ++ch) {
-        const int s = ch % C::NST;
-        if (!wait_or_abort(&c_empty[s], ((ch / C::NST) & 1) ^ 1, abort_flag)) { ok = false; break; }
-        mbar_arrive_expect_tx(&c_full[s], 2 * C::CB);
-        for (int part = 0; part < 2; ++part)
-          for (int h = 0; h < C::HALVES; ++h)
-            tma_load_2d(sC + (s * 2 + part) * C::CB + h * C::ATOM, &cmap, h * 64,
-                        (bh * 2 + part) * kpad + ch * C::CH, &c_full[s]);
-        issued = ch + 1;
+      for (int i = 0; ok && i < nitems; ++i) {
+        const int bh = (blockIdx.x + i * gridDim.x) / ntp;
+        for (int ch = 0; ok && ch < nch; ++ch)
+          for (int part = 0; part < 2; ++part) {
+            const int u = 2 * (i * nch + ch) + part, s = u % C::NST;
+            if (!wait_or_abort(&c_empty[s], ((u / C::NST) & 1) ^ 1, abort_flag)) { ok = false; break; }
+            mbar_arrive_expect_tx(&c_full[s], C::CB);
+            for (int h = 0; h < C::HALVES; ++h)
+              tma_load_2d(sC + s * C::CB + h * (C::CH * 128), &cmap, h * 64, (bh * 2 + part) * kpad + ch * C::CH,
+                          &c_full[s]);
+            issued = u + 1;
+          }
       }
       if (!ok) fail(status, abort_flag);
-      // Teardown: every load issued into this CTA's shared memory has landed.
-      bool done = mbar_wait(x_full, 0, kWaitLimit);
-      for (int ch = issued > C::NST ? issued - C::NST : 0; ch < issued; ++ch)
-        done &= mbar_wait(&c_full[ch % C::NST], (ch / C::NST) & 1, kWaitLimit);
+      bool done = true;
+      for (int u = issued > C::NST ? issued - C::NST : 0; u < issued; ++u)
+        done &= mbar_wait(&c_full[u % C::NST], (u / C::NST) & 1, kWaitLimit);
       if (!done) fail(status, abort_flag);
     }
   } else if (warp == 9) {
@@ -205,34 +238,40 @@ __global__ void __launch_bounds__(320, 1)
     auto wwait = [&](uint64_t* bar, uint32_t parity) {
       return __all_sync(0xffffffffu, wait_or_abort(bar, parity, abort_flag));
     };
-    bool ok = wwait(x_full, 0);
-    for (int ch = 0; ok && ch < nch; ++ch) {
-      const int s = ch % C::NST, b = ch & 1;
-      if (!wwait(&c_full[s], (ch / C::NST) & 1) || !wwait(&acc_empty[b], ((ch >> 1) & 1) ^ 1)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      if (leader) {
+    bool ok = true;
+    for (int i = 0; ok && i < nitems; ++i) {
+      const int xb = i % C::NXB;
+      if (!wwait(&x_full[xb], (i / C::NXB) & 1)) { ok = false; break; }
+      for (int ch = 0; ok && ch < nch; ++ch) {
+        const int c = i * nch + ch, b = c & 1;
+        if (!wwait(&acc_empty[b], ((c >> 1) & 1) ^ 1)) { ok = false; break; }
+        for (int part = 0; part < 2; ++part) {
+          const int u = 2 * c + part, s = u % C::NST;
+          if (!wwait(&c_full[s], (u / C::NST) & 1)) { ok = false; break; }
+          tc_fence_after();
+          if (leader) {
 #pragma unroll
-        for (int g = 0; g < C::TPC; ++g) {
-          const uint32_t d = tmem + (uint32_t)((g * 2 + b) * C::CH);
+            for (int g = 0; g < C::TPC; ++g) {
+              const uint32_t d = tmem + (uint32_t)((g * 2 + b) * C::CH);
 #pragma unroll
-          for (int part = 0; part < 2; ++part) {
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              // K step of 16 bf16 = 32 bytes inside a 128-byte swizzle atom; a new atom every 4
-              const uint64_t koff = (uint64_t)((kk >> 2) * (C::ATOM >> 4) + 2 * (kk & 3));
-              const uint64_t a = dx0 + (uint64_t)(g * (C::XT >> 4)) + koff;
-              const uint64_t bd = dc0 + (uint64_t)((s * 2 + part) * (C::CB >> 4)) + koff;
-              mma_bf16_ss(d, a, bd, idesc, (part | kk) ? 1u : 0u);
+              for (int kk = 0; kk < D / 16; ++kk) {
+                // K step of 16 bf16 = 32 bytes inside a 128-byte swizzle atom; a new atom every 4
+                const uint64_t kx = (uint64_t)((kk >> 2) * (C::ATOM >> 4) + 2 * (kk & 3));
+                const uint64_t kc = (uint64_t)((kk >> 2) * ((C::CH * 128) >> 4) + 2 * (kk & 3));
+                const uint64_t a = dx0 + (uint64_t)((xb * C::TPC + g) * (C::XT >> 4)) + kx;
+                const uint64_t bd = dc0 + (uint64_t)(s * (C::CB >> 4)) + kc;
+                mma_bf16_ss(d, a, bd, idesc, (part | kk) ? 1u : 0u);  // hi, then lo onto it
+              }
+            }
+            mma_commit(&c_empty[s]);
+            if (part == 1) {
+              mma_commit(&acc_full[b]);
+              if (ch == nch - 1) mma_commit(&x_empty[xb]);  // the item's token tiles are no longer read
             }
           }
+          __syncwarp();
         }
-        mma_commit(&c_empty[s]);
-        mma_commit(&acc_full[b]);
       }
-      __syncwarp();
     }
     if (!ok && lane == 0) fail(status, abort_flag);
     if (leader) mma_commit(drain);
@@ -242,52 +281,55 @@ __global__ void __launch_bounds__(320, 1)
     // ---------------------------------------------------------------- argmin epilogue, warps 0-7
     const int g = warp >> 2, wq = warp & 3;
     const int row = wq * 32 + lane;
-    const int tok = t0 + g * 128 + row;
     const uint32_t tbase = tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(g * 2 * C::CH);
-    const float* cn = cnormp + (int64_t)bh * kpad;
-    float best = INFINITY;
-    int bi = 0;
     bool ok = true;
-    for (int ch = 0; ch < nch; ++ch) {
-      const int b = ch & 1;
-      const bool got = wait_or_abort(&acc_full[b], (ch >> 1) & 1, abort_flag);
-      if (!__all_sync(0xffffffffu, got)) {
-        if (lane == 0) fail(status, abort_flag);
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      // All 128 dot products of the chunk in one round trip; the buffer is released before the scan.
-      uint32_t r[C::CH];
+    for (int i = 0; ok && i < nitems; ++i) {
+      const int w = blockIdx.x + i * gridDim.x;
+      const int bh = w / ntp, tok = (w % ntp) * C::TPC * 128 + g * 128 + row;
+      const float* cn = cnormp + (int64_t)bh * kpad;
+      float best = INFINITY;
+      int bi = 0;
+      for (int ch = 0; ch < nch; ++ch) {
+        const int c = i * nch + ch, b = c & 1;
+        const bool got = wait_or_abort(&acc_full[b], (c >> 1) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, got)) {
+          if (lane == 0) fail(status, abort_flag);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // All dot products of the chunk in one round trip; the buffer is released before the scan.
+        uint32_t r[C::CH];
 #pragma unroll
-      for (int c0 = 0; c0 < C::CH; c0 += 32)
-        tmem_ld32(tbase + (uint32_t)(b * C::CH + c0), *reinterpret_cast<uint32_t(*)[32]>(&r[c0]));
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&acc_empty[b]);
-      const float4* cn4 = reinterpret_cast<const float4*>(cn + ch * C::CH);
+        for (int c0 = 0; c0 < C::CH; c0 += 32)
+          tmem_ld32(tbase + (uint32_t)(b * C::CH + c0), *reinterpret_cast<uint32_t(*)[32]>(&r[c0]));
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&acc_empty[b]);
+        const float4* cn4 = reinterpret_cast<const float4*>(cn + ch * C::CH);
 #pragma unroll
-      for (int q = 0; q < C::CH / 4; ++q) {
-        const float4 n4 = __ldg(cn4 + q);
-        const float nn[4] = {n4.x, n4.y, n4.z, n4.w};
+        for (int q = 0; q < C::CH / 4; ++q) {
+          const float4 n4 = __ldg(cn4 + q);
+          const float nn[4] = {n4.x, n4.y, n4.z, n4.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float dist = fmaf(-2.f, __uint_as_float(r[4 * q + e]), nn[e]);
-          if (dist < best) {  // ascending scan: a tie keeps the lower index
-            best = dist;
-            bi = ch * C::CH + 4 * q + e;
+          for (int e = 0; e < 4; ++e) {
+            const float dist = fmaf(-2.f, __uint_as_float(r[4 * q + e]), nn[e]);
+            if (dist < best) {  // ascending scan: a tie keeps the lower index
+              best = dist;
+              bi = ch * C::CH + 4 * q + e;
+            }
           }
         }
       }
+      if (ok && tok < S) labels[(int64_t)bh * S + tok] = bi;
     }
-    if (ok && tok < S) labels[(int64_t)bh * S + tok] = bi;
   }
 
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
@@ -487,15 +529,21 @@ int launch_kmeans(const PlanBuffers& p, const uint16_t* V, int iters, bool warm,
                      (uint64_t)D * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc == VC_OK)
     rc = encode_2d(&cmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.cent16, D, (uint64_t)BH * 2 * kpad, (uint64_t)D * 2,
-                   64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+                   64, C::CH, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != VC_OK) return rc;
   const dim3 gc((kpad + 7) / 8, BH), gu((k + 7) / 8, BH);
-  const dim3 ga((S + C::TPC * 128 - 1) / (C::TPC * 128), BH);
+  // Persistent assignment: one CTA per SM (all of an SM's shared memory), items spread round-robin.
+  int dev = 0, nsm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) !=
+                                                cudaSuccess)
+    return VC_ERR_CUDA;
+  const int nwork = (S + C::TPC * 128 - 1) / (C::TPC * 128) * BH;
+  const int ga = nwork < nsm ? nwork : nsm;
   const dim3 gh(p.nchunk, BH);
   // Warm start: the centroids of the plan's previous grouping (and their splits and norms) stay.
   if (!warm) kmeans_init_kernel<D><<<gc, 256, 0, st>>>(V, S, k, kpad, p.cent, p.cnorm, p.cent16, p.cnormp);
   for (int it = 0; it < iters; ++it) {
-    kmeans_assign_kernel<D><<<ga, 320, C::SMEM, st>>>(xmap, cmap, p.cnormp, S, kpad, p.labels, p.status);
+    kmeans_assign_kernel<D><<<ga, 352, C::SMEM, st>>>(xmap, cmap, p.cnormp, S, kpad, nwork, p.labels, p.status);
     label_hist_kernel<<<gh, 256, 0, st>>>(p.labels, S, k, p.nchunk, p.chist);
     label_scan_kernel<<<BH, 1024, 0, st>>>(k, p.nchunk, p.chist, p.counts, p.offsets);
     label_scatter_kernel<<<gh, 256, 0, st>>>(p.labels, S, k, p.nchunk, p.chist, p.perm);
