@@ -434,7 +434,14 @@ def main():
         b.record(s_in)
         torch.cuda.synchronize()
         h2d_gbs = Q.numel() * Q.element_size() / (a.elapsed_time(b) * 1e-3) / 1e9
-        n_e2e = max(2, min(args.steps, 5))
+        a.record(s_out)
+        with torch.cuda.stream(s_out):
+            Oh[0].copy_(Od[0], non_blocking=True)
+        b.record(s_out)
+        torch.cuda.synchronize()
+        d2h_gbs = O.numel() * O.element_size() / (a.elapsed_time(b) * 1e-3) / 1e9
+        # enough steps that the pipeline's fill (step 0's inputs) and drain (the last output) are small
+        n_e2e = max(2, min(max(args.steps, 10), 20))
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier()
         a.record(s_in)
@@ -449,7 +456,7 @@ def main():
                "h2d_bytes_per_step": 3 * nbytes, "d2h_bytes_per_step": nbytes,
                "copies": "own streams, double-buffered: step i+1's inputs and step i-1's output move while step i "
                          "computes",
-               "h2d_gbs_alone": h2d_gbs, "host_cores": placement}
+               "steps": n_e2e, "h2d_gbs_alone": h2d_gbs, "d2h_gbs_alone": d2h_gbs, "host_cores": placement}
         del Qh, Kh, Vh, Oh, Qd, Kd, Vd, Od
         os.sched_setaffinity(0, all_cores)
 
