@@ -58,6 +58,22 @@ def head_of(a: dict, b: int, h: int) -> dict:
     return g
 
 
+def gpu_plan_one_head(m, plan, b, h) -> dict:
+    """The prepare outputs of one batch-head, sliced on the device before the copy (large plans)."""
+    def get(what):
+        t = m.vc_plan_get(plan, what)[b, h]
+        torch.cuda.synchronize()
+        return u16(t) if t.dtype == torch.bfloat16 else t.cpu().numpy()
+
+    g = {key: get(what) for key, what in (("perm", m.VC_PLAN_PERM), ("labels", m.VC_PLAN_LABELS),
+                                          ("qc", m.VC_PLAN_QCODES), ("sq", m.VC_PLAN_QSCALES),
+                                          ("kc", m.VC_PLAN_KCODES), ("sk", m.VC_PLAN_KSCALES),
+                                          ("mub", m.VC_PLAN_MEANS))}
+    g["rc"] = np.ascontiguousarray(get(m.VC_PLAN_VCODES).T)
+    g["sv"] = float(get(m.VC_PLAN_VSCALES))
+    return g
+
+
 def gpu_plan_head(m, plan, b, h) -> dict:
     """The GPU's prepare outputs for one batch-head (copies the whole plan: small plans only)."""
     return head_of(gpu_plan_all(m, plan), b, h)

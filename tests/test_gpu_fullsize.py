@@ -13,7 +13,8 @@ import torch
 
 import oracle
 import synth
-from gpu_helpers import assert_within, compare_prep, f64, gpu_plan_all, head_of, oracle_forward_from_plan, u16, vc
+from gpu_helpers import (assert_within, compare_prep, f64, gpu_plan_all, gpu_plan_one_head, head_of,
+                         oracle_forward_from_plan, u16, vc)
 
 pytestmark = pytest.mark.gpu
 
@@ -133,4 +134,34 @@ def test_wan_fullsize_channel_scale_and_k_centering(m):
         ref = oracle.attention_quant(g["qc"], g["sq"], g["kc"], g["sk"], g["rc"], svc[0, h], g["mub"], S, rows,
                                      mut=mt[0, h, :, :nkb].T)[0]
         assert_within(f64(O[0, h])[rows], ref, float(np.abs(f64(V[0, h])).max()), f"channel head {h}")
+    plan.destroy()
+
+
+def test_maximum_sequence_length_past_two_gig_elements(m):
+    """The largest S and k the boundary accepts (2^20 tokens, 1024 clusters), with enough heads that every
+    per-tensor element count passes 2^31 (17 * 2^20 * 128): the last head's codes, means and output sit past
+    the 32-bit offset range. Inputs are seeded Gaussians drawn on the device (q, k std 0.5, v std 1) with one
+    token in 200 of V scaled by 30, as outlier rows."""
+    S, H, D, k = 1 << 20, 17, 128, 1024
+    gen = torch.Generator(device="cuda").manual_seed(11)
+    Q = (0.5 * torch.randn(1, H, S, D, device="cuda", generator=gen)).to(torch.bfloat16)
+    K = (0.5 * torch.randn(1, H, S, D, device="cuda", generator=gen)).to(torch.bfloat16)
+    V = torch.randn(1, H, S, D, device="cuda", generator=gen)
+    V[:, :, torch.randperm(S, device="cuda", generator=gen)[:S // 200]] *= 30.0
+    V = V.to(torch.bfloat16)
+    plan = m.vc_attn_prepare(Q, K, V, k, 1)
+    O = m.vc_attn_forward(plan)
+    torch.cuda.synchronize()
+    assert m.vc_plan_status(plan) == (0, 0)
+    rng = np.random.default_rng(12)
+    for h, prep in ((H - 1, True), (0, False)):
+        g = gpu_plan_one_head(m, plan, 0, h)
+        assert np.array_equal(g["perm"], oracle.stable_argsort(g["labels"], k)), f"head {h}"
+        if prep:
+            o = oracle.prepare_head(u16(Q[0, h]), u16(K[0, h]), u16(V[0, h]), k, 1, perm=g["perm"])
+            compare_prep(g, o, S)
+        rows = np.unique(np.concatenate([rng.choice(S, 3, replace=False), [S - 1]]))
+        ref = oracle_forward_from_plan(g, S, rows)
+        got = f64(O[0, h][torch.as_tensor(rows, device=O.device)])
+        assert_within(got, ref, float(V[0, h].float().abs().max()), f"max-S head {h}")
     plan.destroy()
