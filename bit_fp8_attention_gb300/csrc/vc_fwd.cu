@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
   uint64_t* q_full = bars;
   uint64_t* k_full = q_full + 1;          // per K pair stage
   uint64_t* k_empty = k_full + C::NKP;
-  uint64_t* v_full = k_empty + C::NKP;
+  uint64_t* v_full = k_empty + C::NKP;    // per V pair slot (the first two of NV barriers): both tiles landed
   uint64_t* mu_full = v_full + C::NV;
   uint64_t* mu_empty = mu_full + C::NMU;
   uint64_t* s_full = mu_empty + C::NMU;   // S pair k landed (one phase per pair)
@@ -220,41 +220,51 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
       issued_mu = q + 1;
       return true;
     };
+    // The two V^T tiles of a pair land on one barrier (v_full[pair % 2]), so the MMA thread waits
+    // once per pair. A pair's slots are refilled once PV of the pair two back has completed.
     bool loads_ok = true;
-    for (int t = 0; t < ntiles && loads_ok; ++t) {
+    for (int t0 = 0; t0 < ntiles && loads_ok; t0 += 2) {
       if (warp_aborted(abort_flag)) { loads_ok = false; break; }
-      const bool regular = !kRepair || t < nkb;
-      const int j = regular ? tile_at(t, start) : t - nkb;
-      if (use_mean && t > 0 && seg_start(t, start) && !load_mean_block(tile_at(t - 1, start) >> 4)) {
-        loads_ok = false;
-        break;
-      }
-      const int sv = t % C::NV;
-      if (t >= C::NV && !leader_wait(&o_done[(t - C::NV) & 3], ((t - C::NV) >> 2) & 1)) { loads_ok = false; break; }
-      {  // one-hot rows (all zero under a repair tile: it adds nothing to the row sums); a constant
-         // row is invariant under the 16-byte chunk swizzle
-        uint4* onehot = reinterpret_cast<uint4*>(sV + sv * C::VSTAGE + C::VB);
+      const int np = t0 + 1 < ntiles ? 2 : 1;
+      for (int t = t0; t < t0 + np; ++t)
+        if (use_mean && t > 0 && seg_start(t, start) && !load_mean_block(tile_at(t - 1, start) >> 4)) {
+          loads_ok = false;
+          break;
+        }
+      if (!loads_ok) break;
+      if (t0 >= C::NV && !leader_wait(&o_done[(t0 - 3) & 3], ((t0 - 3) >> 2) & 1)) { loads_ok = false; break; }
+      for (int t = t0; t < t0 + np; ++t) {  // one-hot rows (all zero under a repair tile: it adds nothing to
+                                            // the row sums); a constant row is invariant under the swizzle
+        const bool regular = !kRepair || t < nkb;
+        const int j = regular ? tile_at(t, start) : t - nkb;
+        uint4* onehot = reinterpret_cast<uint4*>(sV + (t % C::NV) * C::VSTAGE + C::VB);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int i = lane + 32 * q;
           const uint32_t v = (regular && (i >> 3) == (j & 15)) ? 0x38383838u : 0u;
           onehot[i] = make_uint4(v, v, v, v);
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
       }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
       if (leader) {
-        mbar_arrive_expect_tx(&v_full[sv], C::VB);
-        tma_load_2d(sV + sv * C::VSTAGE, regular ? &maps.v : &maps.vrep, j * 128, bh * D, &v_full[sv]);
+        uint64_t* bar = &v_full[(t0 >> 1) & 1];
+        mbar_arrive_expect_tx(bar, np * C::VB);
+        for (int t = t0; t < t0 + np; ++t) {
+          const bool regular = !kRepair || t < nkb;
+          const int j = regular ? tile_at(t, start) : t - nkb;
+          tma_load_2d(sV + (t % C::NV) * C::VSTAGE, regular ? &maps.v : &maps.vrep, j * 128, bh * D, bar);
+        }
       }
-      issued_v = t + 1;
+      issued_v = t0 + np;
     }
     if (loads_ok && use_mean && !load_mean_block(tile_at(nkb - 1, start) >> 4)) loads_ok = false;  // the last run
     if (!loads_ok && leader) record_failure(args.status, abort_flag, kStatusTimeoutLoad);
     if (leader) {
       bool ok = true;
-      for (int t = max(0, issued_v - C::NV); t < issued_v; ++t)
-        ok &= mbar_wait(&v_full[t % C::NV], (t / C::NV) & 1, kWaitLimit);
+      const int issued_pairs = (issued_v + 1) / 2;
+      for (int k = max(0, issued_pairs - 2); k < issued_pairs; ++k)
+        ok &= mbar_wait(&v_full[k & 1], (k >> 1) & 1, kWaitLimit);
       for (int q = max(0, issued_mu - C::NMU); q < issued_mu; ++q)
         ok &= mbar_wait(&mu_full[q % C::NMU], (q / C::NMU) & 1, kWaitLimit);
       if (!ok) record_failure(args.status, abort_flag, kStatusTimeoutDrain);
@@ -342,12 +352,14 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
           ++seg;
         }
         const int sv = t % C::NV;
-        if (!warp_wait(&v_full[sv], (t / C::NV) & 1, kWaitLimit, abort_flag)) {
-          fail(kStatusTimeoutLoad);
-          ok = false;
-          break;
+        if (g == 0) {  // both V^T tiles of the pair
+          if (!warp_wait(&v_full[(t >> 1) & 1], (t >> 2) & 1, kWaitLimit, abort_flag)) {
+            fail(kStatusTimeoutLoad);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
         }
-        tc_fence_after();
         if (leader) {
           const uint32_t tP = g ? tP1 : tP0;
           const uint64_t dv = dv0 + (uint64_t)(sv * (C::VSTAGE >> 4));
