@@ -1,7 +1,9 @@
 """Build the sm_103a library in-tree: csrc/*.cu -> _build/libvc_attn.so (nvcc, one -gencode).
 
 Each translation unit is compiled in parallel; the link step produces one shared library with
-the C ABI of include/vc_attn.h. Run as `python -m bit_fp8_attention_gb300.build`.
+the C ABI of include/vc_attn.h. The FP8 tensor-core rate probe that the benchmark uses for its
+roofline (probe/fp8_mma_peak.cu) is built beside it as _build/libvc_probe.so; it is measurement
+support, not part of the attention library. Run as `python -m bit_fp8_attention_gb300.build`.
 """
 from __future__ import annotations
 
@@ -16,6 +18,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libvc_attn.so")
+PROBE_SRC = os.path.join(PKG, "probe", "fp8_mma_peak.cu")
+PROBE_LIB = os.path.join(OUT, "libvc_probe.so")
 NVCC = os.environ.get("NVCC", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", f"-I{os.path.join(ROOT, 'include')}"]
@@ -35,6 +39,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
                      [os.path.join(ROOT, "include", "vc_attn.h")])
     objs = []
     jobs = []
+    probe_deps = [PROBE_SRC, os.path.join(CSRC, "vc_device.cuh")]
+    if force or _stale(PROBE_LIB, probe_deps):
+        jobs.append([NVCC, *ARCH, *FLAGS, "-shared", PROBE_SRC, "-o", PROBE_LIB])
     for src in sources:
         obj = os.path.join(OUT, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)

@@ -125,7 +125,9 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base + C::OFF_MISC + 8);
   float* mbuf = reinterpret_cast<float*>(base + C::OFF_MBUF);
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // The warp index read back from lane 0 is one the compiler knows to be warp-uniform: each role's
+  // loop state and the MMA descriptors then live in uniform registers.
+  const int tid = threadIdx.x, warp = __shfl_sync(0xffffffffu, tid >> 5, 0), lane = tid & 31;
   const int qt = blockIdx.x, bh = blockIdx.y;
   const int nkb = args.nkb;
   // Positions 0..nkb-1 visit the regular key tiles in the chosen order, positions nkb..ntiles-1 the

@@ -158,7 +158,9 @@ __global__ void __launch_bounds__(352, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base + C::OFF_MISC + 8);
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // The warp index read back from lane 0 is one the compiler knows to be warp-uniform: each role's
+  // loop state and the MMA descriptors then live in uniform registers.
+  const int tid = threadIdx.x, warp = __shfl_sync(0xffffffffu, tid >> 5, 0), lane = tid & 31;
   const int ntp = (S + C::TPC * 128 - 1) / (C::TPC * 128);  // work items per head
   const int nch = kpad / C::CH;
   const int nitems = nwork > (int)blockIdx.x ? (nwork - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;

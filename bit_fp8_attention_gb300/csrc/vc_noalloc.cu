@@ -8,36 +8,27 @@
 // library's own device memory, sized for at most VC_NOALLOC_MAX_HEADS batch-heads (16 KiB, held by
 // every GPU that loads the library until the process exits).
 #include <cuda_runtime.h>
-#include <mutex>
 #include <stdint.h>
 
 #include "vc_internal.h"
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-
 // Per-head residual maxima (as float bit patterns) shared by every call on a device.
 static __device__ __align__(256) unsigned int g_residual_amax[VC_NOALLOC_MAX_HEADS];
 
-std::mutex g_setup_mutex;
-unsigned int* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device, looked up once per device. In host
-// code `g_residual_amax` only names a host-side stand-in, so the address must come from the runtime.
+// Device address of the scratch array on the current device. In host code `g_residual_amax` only
+// names a host-side stand-in, so the address must come from the runtime. It is looked up on every
+// call (a table lookup once the module is loaded, and no allocation): a cached address would go
+// stale if the caller reset the device (cudaDeviceReset) and the module were loaded again. The
+// first call on a device also loads the library's module there.
 int scratch_for_current_device(unsigned int** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return VC_ERR_NO_DEVICE;
-  std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_residual_amax) != cudaSuccess || p == nullptr) {
-      cudaGetLastError();
-      return VC_ERR_CUDA;
-    }
-    g_scratch_ptr[dev] = static_cast<unsigned int*>(p);
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_residual_amax) != cudaSuccess || p == nullptr) {
+    cudaGetLastError();
+    return VC_ERR_CUDA;
   }
-  *out = g_scratch_ptr[dev];
+  *out = static_cast<unsigned int*>(p);
   return VC_OK;
 }
 
@@ -47,6 +38,7 @@ extern "C" int vc_residual_pack_noalloc(const void* V, const int32_t* perm, int 
                                         uint8_t* vcodes, float* vscales, cudaStream_t stream) {
   if (!V || !means || !vcodes || !vscales) return VC_ERR_INVALID_ARG;
   if (((uintptr_t)V & 15u) || ((uintptr_t)means & 15u) || ((uintptr_t)vcodes & 15u)) return VC_ERR_INVALID_ARG;
+  if (((uintptr_t)perm & 3u) || ((uintptr_t)vscales & 3u)) return VC_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || S < 1) return VC_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return VC_ERR_UNSUPPORTED;
   if ((int64_t)B * H > VC_NOALLOC_MAX_HEADS) return VC_ERR_UNSUPPORTED;  // beyond the fixed scratch

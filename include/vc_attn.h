@@ -225,16 +225,19 @@ int vc_expcast_encode(const float* s, const float* a, const float* b, int64_t n,
  * gather V' = V[pi], the bf16 means of its 128-row blocks and the per-head E4M3 residual codes,
  * transposed and zero-padded -- exactly as vc_attn_prepare_ex writes them into a plan
  * (VC_PLAN_MEANS, VC_PLAN_VCODES, VC_PLAN_VSCALES), into buffers the caller provides.
- * V: device bf16 [B, H, S, D]; perm: device int32 [B, H, S] (entries in [0, S)) or NULL for the
- * identity; means: device bf16 [B, H, ceil(S/128), D]; vcodes: device uint8 [B, H, D, S_pad];
- * vscales: device fp32 [B, H]. V, means and vcodes must be 16-byte aligned.
+ * V: device bf16 [B, H, S, D]; perm: device int32 [B, H, S] or NULL for the identity; means: device
+ * bf16 [B, H, ceil(S/128), D]; vcodes: device uint8 [B, H, D, S_pad]; vscales: device fp32 [B, H].
+ * V, means and vcodes must be 16-byte aligned, perm and vscales 4-byte aligned (else
+ * VC_ERR_INVALID_ARG). Each row of perm must be a permutation of [0, S): an entry outside that range
+ * is not checked and makes the gather read outside V (undefined behaviour).
  * It calls no cudaMalloc, cudaFree or allocating library routine. Its only scratch (one word per
  * batch-head) is a fixed array inside the library, VC_NOALLOC_MAX_HEADS words per GPU, kept until
- * the process exits: B*H above that limit returns VC_ERR_UNSUPPORTED. The first call on a device
- * looks up that array's device address (once per device, with that device current); make that
- * first call before any stream capture. Each call clears the scratch on `stream` before use, but
- * all calls share it: calls that overlap on the GPU (other streams, other host threads) race and
- * must be serialised by the caller. */
+ * the process exits: B*H above that limit returns VC_ERR_UNSUPPORTED. Every call looks up that
+ * array's address on the current device (no allocation; it stays valid across a device reset); the
+ * first call on a device also loads the library's module there, so make that first call before any
+ * stream capture. Each call clears the scratch on `stream` before use, but all calls share it: calls
+ * that overlap on the GPU (other streams, other host threads) race and must be serialised by the
+ * caller. */
 #define VC_NOALLOC_MAX_HEADS 4096
 int vc_residual_pack_noalloc(const void* V, const int32_t* perm, int B, int H, int S, int D, void* means,
                              uint8_t* vcodes, float* vscales, cudaStream_t stream);
