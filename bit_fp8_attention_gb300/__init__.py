@@ -61,6 +61,7 @@ VC_STEP_GROUP, VC_STEP_GROUP_WARM, VC_STEP_REUSE, VC_STEP_PLAIN = 0, 1, 2, 3
 
 EXPORTS = ("vc_attn_prepare", "vc_attn_prepare_ex", "vc_attn_prepare_repair", "vc_attn_forward", "vc_plan_size",
            "vc_plan_get", "vc_plan_status", "vc_plan_shape", "vc_plan_destroy", "vc_expcast_encode",
+           "vc_expcast_encode_unclamped",
            "vc_schedule_action",
            "vc_strerror", "vc_version")
 
@@ -94,6 +95,7 @@ def lib() -> ctypes.CDLL:
         "vc_plan_shape": (i, [vp] + [ctypes.POINTER(i)] * 5),
         "vc_plan_destroy": (None, [vp]),
         "vc_expcast_encode": (i, [vp, vp, vp, ctypes.c_int64, vp, vp]),
+        "vc_expcast_encode_unclamped": (i, [vp, vp, vp, ctypes.c_int64, vp, vp]),
         "vc_residual_pack_noalloc": (i, [vp, vp, i, i, i, i, vp, vp, vp, vp]),
         "vc_schedule_action": (i, [i, i, i]),
         "vc_strerror": (ctypes.c_char_p, [i]),
@@ -303,12 +305,20 @@ def vc_residual_pack_noalloc(V, perm, means, vcodes, vscales, stream=None):
                                           vscales.data_ptr(), _stream(stream)), "vc_residual_pack_noalloc")
 
 
-def vc_expcast_encode(s, a, b, stream=None):
-    """ExpCast-FP8 codes clip[0,120](rne(fmaf(s, a, b))) through the forward kernel's code path."""
+def vc_expcast_encode(s, a, b, stream=None, clamp: bool = True):
+    """ExpCast-FP8 codes clip[0,120](rne(fmaf(s, a, b))) through the forward kernel's code path.
+
+    clamp=False: vc_expcast_encode_unclamped, the bytes of the forward's fast path (no clamp at 120)."""
     for t in (s, a, b):
         if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous() and t.numel() == s.numel()):
             raise ValueError("s, a, b must be contiguous CUDA float32 tensors of equal size")
     out = torch.empty(s.shape, dtype=torch.uint8, device=s.device)
-    _check(lib().vc_expcast_encode(s.data_ptr(), a.data_ptr(), b.data_ptr(), s.numel(), out.data_ptr(),
-                                   _stream(stream)), "vc_expcast_encode")
+    fn = lib().vc_expcast_encode if clamp else lib().vc_expcast_encode_unclamped
+    _check(fn(s.data_ptr(), a.data_ptr(), b.data_ptr(), s.numel(), out.data_ptr(), _stream(stream)),
+           "vc_expcast_encode" if clamp else "vc_expcast_encode_unclamped")
     return out
+
+
+def vc_expcast_encode_unclamped(s, a, b, stream=None):
+    """The forward's fast-path bytes: the code path of vc_expcast_encode without the clamp at 120."""
+    return vc_expcast_encode(s, a, b, stream=stream, clamp=False)

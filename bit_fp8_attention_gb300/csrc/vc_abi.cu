@@ -300,7 +300,15 @@ int vc_expcast_encode(const float* s, const float* a, const float* b, int64_t n,
   if (n < 0 || (n > 0 && (!s || !a || !b || !out))) return VC_ERR_INVALID_ARG;
   int rc = check_device();
   if (rc != VC_OK) return rc;
-  return vc::expcast_launch(s, a, b, n, out, stream);
+  return vc::expcast_launch(s, a, b, n, out, stream, true);
+}
+
+int vc_expcast_encode_unclamped(const float* s, const float* a, const float* b, int64_t n, uint8_t* out,
+                                cudaStream_t stream) {
+  if (n < 0 || (n > 0 && (!s || !a || !b || !out))) return VC_ERR_INVALID_ARG;
+  int rc = check_device();
+  if (rc != VC_OK) return rc;
+  return vc::expcast_launch(s, a, b, n, out, stream, false);
 }
 
 const char* vc_strerror(int status) {

@@ -55,7 +55,7 @@ struct FwdCfg {
   static constexpr int OFF_V = OFF_K + NKP * KPB;
   static constexpr int OFF_MU = OFF_V + NV * VSTAGE;
   static constexpr int OFF_BAR = OFF_MU + NMU * MUB;
-  static constexpr int NBAR = 1 + 2 * NKP + NV + 2 * NMU + 1 + 1 + 2 + 4 + 1 + 1 + 32;
+  static constexpr int NBAR = 1 + NKP + NV + 2 * NMU + 1 + 1 + 2 + 4 + 1 + 1 + 32;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int OFF_MBUF = OFF_MISC + 64;       // tile maxima hand-off, 8 slots x 128 floats
   static constexpr int SMEM = OFF_MBUF + 4096 + 1024;  // + slack for aligning the base to 1024
@@ -69,8 +69,10 @@ struct FwdCfg {
   static constexpr uint32_t T_O = 0, T_W = D, T_F = D + 16, T_L = D + 32, T_P0 = 176, T_P1 = 208, T_S = 256;
 };
 
-// Single-score export: the forward's four-score code path, clamped at 120 afterwards so that it
-// matches the clip of Eq. 7 for every input (the forward never needs the clamp).
+// Single-score export of the forward's four-score code path. kClamp: clamped at 120 afterwards, so
+// that it matches the clip of Eq. 7 for every input. Without the clamp it writes exactly the bytes the
+// forward's fast path writes (the forward skips the clamp while |M| < 2^22, where no code needs it).
+template <bool kClamp>
 __global__ void expcast_kernel(const float* __restrict__ s, const float* __restrict__ a, const float* __restrict__ b,
                                int64_t n, uint8_t* __restrict__ out) {
   int64_t i0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
@@ -85,9 +87,10 @@ __global__ void expcast_kernel(const float* __restrict__ s, const float* __restr
   }
   uint32_t d = expcast4(sv[0], sv[1], sv[2], sv[3], pack2f(av[0], av[1]), pack2f(av[2], av[3]), pack2f(bv[0], bv[1]),
                         pack2f(bv[2], bv[3]));
+  if (kClamp) d = __vminu4(d, 0x78787878u);
 #pragma unroll
   for (int q = 0; q < 4; ++q)
-    if (i0 + q < n) out[i0 + q] = (uint8_t)min((d >> (8 * q)) & 0xFFu, 120u);
+    if (i0 + q < n) out[i0 + q] = (uint8_t)((d >> (8 * q)) & 0xFFu);
 }
 
 template <int D, bool kExpCast, bool kRepair>
@@ -101,13 +104,14 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
   uint8_t* sMu = base + C::OFF_MU;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::OFF_BAR);
   uint64_t* q_full = bars;
-  uint64_t* k_full = q_full + 1;          // per K pair stage
-  uint64_t* k_empty = k_full + C::NKP;
-  uint64_t* v_full = k_empty + C::NKP;    // per V pair slot (the first two of NV barriers): both tiles landed
+  uint64_t* k_full = q_full + 1;          // per K pair stage (a stage is free again once S of its pair is)
+  uint64_t* v_full = k_full + C::NKP;     // per V pair slot (the first two of NV barriers): both tiles landed
   uint64_t* mu_full = v_full + C::NV;
   uint64_t* mu_empty = mu_full + C::NMU;
   uint64_t* s_full = mu_empty + C::NMU;   // S pair k landed (one phase per pair)
-  uint64_t* s_free = s_full + 1;          // both groups hold S pair k in registers (256 arrivals)
+  // s_free phase k: both groups hold S pair k in registers (256 arrivals) and the K tiles of pair k+1
+  // have landed (one arrival by the K producer), so the MMA thread learns both from one wait.
+  uint64_t* s_free = s_full + 1;
   uint64_t* p_full = s_free + 1;          // per group: P of its tile written, O/W/l up to date
   // o_done[t & 3] completes when PV(t) and every earlier MMA are done. Parity waits only tell the
   // current phase from the previous one, so a wait for PV(v) must never find PV(v+4) complete too.
@@ -140,11 +144,11 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
 
   if (tid == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < C::NKP; ++s) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
+    for (int s = 0; s < C::NKP; ++s) mbar_init(&k_full[s], 1);
     for (int s = 0; s < C::NV; ++s) mbar_init(&v_full[s], 1);
     for (int s = 0; s < C::NMU; ++s) { mbar_init(&mu_full[s], 1); mbar_init(&mu_empty[s], 1); }
     mbar_init(s_full, 1);
-    mbar_init(s_free, 256);
+    mbar_init(s_free, 257);
     mbar_init(&p_full[0], 128);
     mbar_init(&p_full[1], 128);
     for (int i = 0; i < 4; ++i) mbar_init(&o_done[i], 1);
@@ -162,7 +166,10 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
   if (warp == 8) {
     // ------------------------------------------------------------------ K producer
     // Q once, then the two key tiles of every S pair into a 2-stage ring; independent of the V
-    // ring, so the next pair is always in flight well before the MMA issuer needs it.
+    // ring, so the next pair is always in flight well before the MMA issuer needs it. The stage of
+    // pair k-2 is free once S pair k-2 has landed (s_full), which the MMA thread committed after
+    // its last read of the stage. Once pair k has landed, the producer adds its arrival to s_free's
+    // phase k-1 (after which the MMA thread issues S pair k).
     if (lane == 0) {
       prefetch_tmap(&maps.q);
       prefetch_tmap(&maps.k);
@@ -180,11 +187,16 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
         if (*abort_flag) { loads_ok = false; break; }
         const int s = k % C::NKP;
         const int t0 = 2 * k, t1 = 2 * k + 1;
-        if (!wait_or_abort(&k_empty[s], ((k / C::NKP) & 1) ^ 1, kWaitLimit, abort_flag)) { loads_ok = false; break; }
+        if (k >= C::NKP && !wait_or_abort(s_full, (k - C::NKP) & 1, kWaitLimit, abort_flag)) { loads_ok = false; break; }
         mbar_arrive_expect_tx(&k_full[s], t1 < ntiles ? 2 * C::QB : C::QB);
         load_k(sK + s * C::KPB, t0, &k_full[s]);
         if (t1 < ntiles) load_k(sK + s * C::KPB + C::QB, t1, &k_full[s]);
         issued_kp = k + 1;
+        if (k >= 1) {  // after phase k-2 of s_free, so that this arrival counts for phase k-1
+          if (k >= 2 && !wait_or_abort(s_free, (k - 2) & 1, kWaitLimit, abort_flag)) { loads_ok = false; break; }
+          if (!wait_or_abort(&k_full[s], (k / C::NKP) & 1, kWaitLimit, abort_flag)) { loads_ok = false; break; }
+          mbar_arrive(s_free);
+        }
       }
       if (!loads_ok) record_failure(args.status, abort_flag, kStatusTimeoutLoad);
       // Teardown: confirm that every load issued into this CTA's shared memory has landed.
@@ -292,16 +304,16 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
     auto fail = [&](int bit) {
       if (lane == 0) record_failure(args.status, abort_flag, bit);
     };
+    // S pair k; for k >= 1 the caller's s_free wait covers the K tiles (see s_free).
     auto issue_qk = [&](int k) -> bool {
       const int s = k % C::NKP;
-      if (!warp_wait(&k_full[s], (k / C::NKP) & 1, kWaitLimit, abort_flag)) return false;
+      if (k == 0 && !warp_wait(&k_full[s], 0, kWaitLimit, abort_flag)) return false;
       tc_fence_after();
       if (leader) {
         const uint64_t dk = dk0 + (uint64_t)(s * (C::KPB >> 4));
 #pragma unroll
         for (int kk = 0; kk < D / 32; ++kk) mma_e4m3_ss(tS, dq + 2 * kk, dk + 2 * kk, id_qk, kk > 0);
         mma_commit(s_full);
-        mma_commit(&k_empty[s]);
       }
       __syncwarp();
       return true;
@@ -800,10 +812,13 @@ int forward_launch(const PlanBuffers& p, const FwdMaps& maps, uint16_t* O, unsig
   return launch_fwd_d<128>(p, maps, O, flags, st);
 }
 
-int expcast_launch(const float* s, const float* a, const float* b, int64_t n, uint8_t* out, cudaStream_t st) {
+int expcast_launch(const float* s, const float* a, const float* b, int64_t n, uint8_t* out, cudaStream_t st,
+                   bool clamp) {
   if (n <= 0) return VC_OK;
   const int64_t threads = (n + 3) / 4;
-  expcast_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(s, a, b, n, out);
+  const unsigned blocks = (unsigned)((threads + 255) / 256);
+  if (clamp) expcast_kernel<true><<<blocks, 256, 0, st>>>(s, a, b, n, out);
+  else expcast_kernel<false><<<blocks, 256, 0, st>>>(s, a, b, n, out);
   return cudaPeekAtLastError() == cudaSuccess ? VC_OK : VC_ERR_CUDA;
 }
 

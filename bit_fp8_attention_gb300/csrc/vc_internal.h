@@ -95,6 +95,7 @@ void quant_blocks_launch(const uint16_t* x, const int32_t* perm, const uint16_t*
 // V residual repair rows (no V-Smooth): energies, selection, copied keys, residual codes. kcen: the K
 // centre or null. The residual maxima (vamax, or vamax_ch when has_vchannel) must be complete.
 int repair_launch(const PlanBuffers& p, const uint16_t* K, const uint16_t* V, const uint16_t* kcen, cudaStream_t st);
-int expcast_launch(const float* s, const float* a, const float* b, int64_t n, uint8_t* out, cudaStream_t st);
+int expcast_launch(const float* s, const float* a, const float* b, int64_t n, uint8_t* out, cudaStream_t st,
+                   bool clamp);
 
 }  // namespace vc

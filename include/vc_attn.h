@@ -216,6 +216,13 @@ void vc_plan_destroy(vc_plan* plan);
 /* ExpCast-FP8 codes (VC-Attention Eq. 7): out[i] = clip[0,120](rne(fmaf(s[i], a[i], b[i]))),
  * computed by the forward kernel's own code path.  s, a, b: device fp32 [n]; out: device u8. */
 int vc_expcast_encode(const float* s, const float* a, const float* b, int64_t n, uint8_t* out, cudaStream_t stream);
+/* The same code path without the final clamp at 120: exactly the bytes the forward writes on its fast
+ * path, which it takes while the running max |M| < 2^22 code units (Open-VC Attention, "Scheduling
+ * around ExpCast": one FMA per score, round, clamp only at 0). With b = 119.65f - M and fl(s*a) <= M
+ * there, every byte equals vc_expcast_encode's; outside that range bytes above 120 may occur (up to
+ * 255). Same arguments and errors as vc_expcast_encode. */
+int vc_expcast_encode_unclamped(const float* s, const float* a, const float* b, int64_t n, uint8_t* out,
+                                cudaStream_t stream);
 
 /* ---- allocation-free variant ----------------------------------------------------------- */
 /* The pages have no counterpart to this call; it exists for callers that must not allocate

@@ -101,6 +101,8 @@ def test_invalid_arguments_rejected_without_device(L):
     L.vc_plan_destroy(None)
     assert L.vc_expcast_encode(None, None, None, 5, None, None) == -1
     assert L.vc_expcast_encode(None, None, None, -1, None, None) == -1
+    assert L.vc_expcast_encode_unclamped(None, None, None, 5, None, None) == -1
+    assert L.vc_expcast_encode_unclamped(None, None, None, -1, None, None) == -1
 
 
 def test_missing_library_fails_loudly(tmp_path, monkeypatch):

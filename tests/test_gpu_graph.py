@@ -38,3 +38,22 @@ def test_prepare_and_forward_replay_in_a_cuda_graph(D, vsmooth):
         assert torch.equal(O, ref), f"seed {seed}"
         fresh.destroy()
     plan.destroy()
+
+
+def test_step_kernel_count_is_counted_from_the_captured_graph():
+    """bench.py reports gpu_launches from the kernel nodes of the captured prepare and forward; they match the
+    step's structure: Q quantisation, k-means initialisation, five kernels per Lloyd round (assignment, label
+    histogram, scan, scatter, update), K' quantisation, block means, residual pack, and the forward."""
+    import bench
+
+    m = vc()
+    cfg = synth.custom(4096, D=128, H=2, k=32, iters=3)
+    Q, K, V = synth.make_inputs(cfg, seed=3, device="cuda")
+    plan = m.vc_attn_prepare(Q, K, V, cfg["k"], cfg["iters"])
+    O = m.vc_attn_forward(plan)
+    torch.cuda.synchronize()
+    n_prep = bench.count_kernels(lambda: m.vc_attn_prepare(Q, K, V, cfg["k"], cfg["iters"], plan=plan))
+    n_fwd = bench.count_kernels(lambda: m.vc_attn_forward(plan, O))
+    assert n_fwd == 1
+    assert n_prep + n_fwd == bench.launches_per_step(cfg)
+    plan.destroy()

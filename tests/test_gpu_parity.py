@@ -44,6 +44,31 @@ def test_expcast_encode_bit_exact(m):
     assert (want == 120).any() and (want == 0).any() and ((want > 0) & (want < 120)).mean() > 0.3
 
 
+def test_expcast_fast_path_bytes_need_no_clamp(m):
+    """The forward writes its codes without the clamp at 120 while |M| < 2^22 (M the running max in code
+    units, every score of the row with fl(s*a) <= M). The unclamped export is that exact code path: on
+    such (s, a, M) its bytes must equal the clipped codes of Eq. 7 ("VC-Attention" Sec. 3.3), including
+    the row maxima themselves (fl(s*a) == M -> 120) and M at the edge of the range."""
+    rng = np.random.default_rng(3)
+    n = 1 << 20
+    a = rng.uniform(1e-3, 2.0, n).astype(np.float32)
+    lim = np.float32(4194304.0)
+    top = rng.uniform(-1.0, 1.0, n) * rng.choice([30.0, 3e3, 4.19e6], n)   # fl(s*a) of the row max
+    s = (top / a).astype(np.float32)
+    sa = (s * a).astype(np.float32)                                       # fp32 product, one rounding
+    gap = np.where(rng.random(n) < 0.25, 0.0, np.abs(rng.normal(0, 40, n)))  # 25%: the score is the max
+    M = (sa + gap).astype(np.float32)
+    M = np.maximum(M, sa)                                                 # fl(s*a) <= M after rounding too
+    keep = np.abs(M) < lim
+    s, a, M = s[keep], a[keep], M[keep]
+    b = (np.float32(119.65) - M).astype(np.float32)
+    assert np.all((s * a).astype(np.float32) <= M)
+    want = oracle.expcast_codes(s, a, b)
+    got = m.vc_expcast_encode(*(torch.from_numpy(x).cuda() for x in (s, a, b)), clamp=False).cpu().numpy()
+    assert np.array_equal(got, want)
+    assert (want == 120).mean() > 0.2 and (want == 0).any() and np.abs(M).max() > 4e6
+
+
 def run(m, cfg, seed=0, vsmooth=True, perm=None):
     Q, K, V = synth.make_inputs(cfg, seed=seed, device="cuda")
     plan = m.vc_attn_prepare_ex(Q, K, V, cfg["k"], cfg["iters"], perm=perm, flags=m.VC_VSMOOTH if vsmooth else 0)
