@@ -112,7 +112,10 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
   // s_free phase k: both groups hold S pair k in registers (256 arrivals) and the K tiles of pair k+1
   // have landed (one arrival by the K producer), so the MMA thread learns both from one wait.
   uint64_t* s_free = s_full + 1;
-  uint64_t* p_full = s_free + 1;          // per group: P of its tile written, O/W/l up to date
+  // p_full[g]: P of group g's tile written, O/W/l up to date (128 arrivals); p_full[0] also counts one
+  // arrival by the V producer once both V^T tiles of the pair have landed, so that one wait of the MMA
+  // thread covers the values of the pair as well.
+  uint64_t* p_full = s_free + 1;
   // o_done[t & 3] completes when PV(t) and every earlier MMA are done. Parity waits only tell the
   // current phase from the previous one, so a wait for PV(v) must never find PV(v+4) complete too.
   // A group at tile t waits only for v > t-5 (every PV up to t-4 is known complete from S, see
@@ -149,7 +152,7 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
     for (int s = 0; s < C::NMU; ++s) { mbar_init(&mu_full[s], 1); mbar_init(&mu_empty[s], 1); }
     mbar_init(s_full, 1);
     mbar_init(s_free, 257);
-    mbar_init(&p_full[0], 128);
+    mbar_init(&p_full[0], 129);
     mbar_init(&p_full[1], 128);
     for (int i = 0; i < 4; ++i) mbar_init(&o_done[i], 1);
     mbar_init(f_full, 128);
@@ -234,11 +237,19 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
       issued_mu = q + 1;
       return true;
     };
-    // The two V^T tiles of a pair land on one barrier (v_full[pair % 2]), so the MMA thread waits
-    // once per pair. A pair's slots are refilled once PV of the pair two back has completed.
+    // The two V^T tiles of a pair land on one barrier (v_full[pair % 2]); once they have, the producer
+    // adds one arrival to the pair's p_full[0] phase, so the MMA thread learns of both from one wait.
+    // A pair's slots are refilled once PV of the pair two back has completed.
+    auto signal_v = [&](int kp) -> bool {
+      if (kp >= 1 && !leader_wait(&p_full[0], (kp - 1) & 1)) return false;  // phase kp-1 done: this counts for kp
+      if (!leader_wait(&v_full[kp & 1], (kp >> 1) & 1)) return false;
+      if (leader) mbar_arrive(&p_full[0]);
+      return true;
+    };
     bool loads_ok = true;
     for (int t0 = 0; t0 < ntiles && loads_ok; t0 += 2) {
       if (warp_aborted(abort_flag)) { loads_ok = false; break; }
+      if (t0 >= 2 && !signal_v(t0 / 2 - 1)) { loads_ok = false; break; }
       const int np = t0 + 1 < ntiles ? 2 : 1;
       for (int t = t0; t < t0 + np; ++t)
         if (use_mean && t > 0 && seg_start(t, start) && !load_mean_block(tile_at(t - 1, start) >> 4)) {
@@ -272,6 +283,7 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
       }
       issued_v = t0 + np;
     }
+    if (loads_ok && issued_v > 0 && !signal_v((issued_v - 1) / 2)) loads_ok = false;
     if (loads_ok && use_mean && !load_mean_block(tile_at(nkb - 1, start) >> 4)) loads_ok = false;  // the last run
     if (!loads_ok && leader) record_failure(args.status, abort_flag, kStatusTimeoutLoad);
     if (leader) {
@@ -366,14 +378,6 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
           ++seg;
         }
         const int sv = t % C::NV;
-        if (g == 0) {  // both V^T tiles of the pair
-          if (!warp_wait(&v_full[(t >> 1) & 1], (t >> 2) & 1, kWaitLimit, abort_flag)) {
-            fail(kStatusTimeoutLoad);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-        }
         if (leader) {
           const uint32_t tP = g ? tP1 : tP0;
           const uint64_t dv = dv0 + (uint64_t)(sv * (C::VSTAGE >> 4));

@@ -74,8 +74,10 @@ __global__ void __launch_bounds__(352, 1) vc_fwd2_kernel(const __grid_constant__
   // Per group g (two each): s_full[g] one phase per score sub-tile, s_free[g] the group holds that
   // sub-tile in registers (128 arrivals), p_full[g] one phase per tile (codes, O/W rescale and F
   // written; 128 arrivals), o_done[g] one phase per PV of the group (and one for its last mean term),
-  // f_full[g] the last run's F (128 arrivals). A phase can never run two ahead of its waiter: each
-  // next phase needs an arrival or an MMA that the waiter's own progress gates.
+  // f_full[g] the last run's F (128 arrivals). s_free[0] phase t also counts one arrival by the K'
+  // producer once tile t+1 has landed, and p_full[0] phase t one by the V producer once V^T tile t has
+  // landed, so that the MMA thread waits for neither load separately. A phase can never run two ahead
+  // of its waiter: each next phase needs an arrival or an MMA that the waiter's own progress gates.
   uint64_t* s_full = mu_empty + C::NMU;
   uint64_t* s_free = s_full + 2;
   uint64_t* p_full = s_free + 2;
@@ -103,8 +105,8 @@ __global__ void __launch_bounds__(352, 1) vc_fwd2_kernel(const __grid_constant__
     for (int s = 0; s < C::NMU; ++s) { mbar_init(&mu_full[s], 1); mbar_init(&mu_empty[s], 1); }
     for (int g = 0; g < 2; ++g) {
       mbar_init(&s_full[g], 1);
-      mbar_init(&s_free[g], 128);
-      mbar_init(&p_full[g], 128);
+      mbar_init(&s_free[g], g == 0 ? 129 : 128);
+      mbar_init(&p_full[g], g == 0 ? 129 : 128);  // group 0's two: + one producer arrival each
       mbar_init(&o_done[g], 1);
       mbar_init(&f_full[g], 128);
     }
@@ -140,6 +142,11 @@ __global__ void __launch_bounds__(352, 1) vc_fwd2_kernel(const __grid_constant__
         if (!kRepair || t < nkb) tma_load_2d(sK + s * C::QB, &maps.k, 0, row0 + tile_at(t, start) * 128, &k_full[s]);
         else tma_load_2d(sK + s * C::QB, &maps.krep, 0, bh * args.R_pad + (t - nkb) * 128, &k_full[s]);
         issued = t + 1;
+        if (t >= 1) {  // tile t landed: one arrival on s_free[0]'s phase t-1 (after phase t-2)
+          if (t >= 2 && !wait_or_abort(&s_free[0], (t - 2) & 1, kWaitLimit, abort_flag)) { loads_ok = false; break; }
+          if (!wait_or_abort(&k_full[s], (t / C::NK) & 1, kWaitLimit, abort_flag)) { loads_ok = false; break; }
+          mbar_arrive(&s_free[0]);
+        }
       }
       if (!loads_ok) record_failure(args.status, abort_flag, kStatusTimeoutLoad);
       bool ok = mbar_wait(q_full, 0, kWaitLimit);
@@ -174,9 +181,16 @@ __global__ void __launch_bounds__(352, 1) vc_fwd2_kernel(const __grid_constant__
       issued_mu = q + 1;
       return true;
     };
+    auto signal_v = [&](int u) -> bool {  // V(u) landed: one arrival on p_full[0]'s phase u
+      if (u >= 1 && !leader_wait(&p_full[0], (u - 1) & 1)) return false;
+      if (!leader_wait(&v_full[u % C::NV], (u / C::NV) & 1)) return false;
+      if (leader) mbar_arrive(&p_full[0]);
+      return true;
+    };
     bool loads_ok = true;
     for (int t = 0; t < ntiles && loads_ok; ++t) {
       if (warp_aborted(abort_flag)) { loads_ok = false; break; }
+      if (t >= 1 && !signal_v(t - 1)) { loads_ok = false; break; }
       const bool regular = !kRepair || t < nkb;  // a repair tile has zero one-hot rows: nothing enters W
       const int j = regular ? tile_at(t, start) : t - nkb;
       if (use_mean && t > 0 && seg_start(t, start) && !load_mean_block(tile_at(t - 1, start) >> 4)) {
@@ -202,6 +216,7 @@ __global__ void __launch_bounds__(352, 1) vc_fwd2_kernel(const __grid_constant__
       }
       issued_v = t + 1;
     }
+    if (loads_ok && issued_v > 0 && !signal_v(issued_v - 1)) loads_ok = false;
     if (loads_ok && use_mean && !load_mean_block(tile_at(nkb - 1, start) >> 4)) loads_ok = false;  // the last run
     if (!loads_ok && leader) record_failure(args.status, abort_flag, kStatusTimeoutLoad);
     if (leader) {
@@ -276,20 +291,12 @@ __global__ void __launch_bounds__(352, 1) vc_fwd2_kernel(const __grid_constant__
       if (leader) mma_commit(&k_empty[t % C::NK]);  // every score MMA of tile t is issued
       __syncwarp();
       if (t + 1 < ntiles) {
-        if (!warp_wait(&k_full[(t + 1) % C::NK], ((t + 1) / C::NK) & 1, kWaitLimit, abort_flag)) {
-          fail(kStatusTimeoutLoad);
-          break;
-        }
         if (!issue_qk(0, t + 1, 0) || !issue_qk(1, t + 1, 0)) {
           fail(kStatusTimeoutP);
           break;
         }
       }
       const int sv = t % C::NV;
-      if (!warp_wait(&v_full[sv], (t / C::NV) & 1, kWaitLimit, abort_flag)) {
-        fail(kStatusTimeoutLoad);
-        break;
-      }
       const bool run = seg_start(t, start);
       for (int g = 0; ok && g < 2; ++g) {
         if (!warp_wait(&p_full[g], t & 1, kWaitLimit, abort_flag)) {
