@@ -58,8 +58,10 @@ struct FwdCfg {
   static constexpr int NBAR = 1 + NKP + NV + 2 * NMU + 1 + 1 + 2 + 4 + 1 + 1 + 32;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int OFF_MBUF = OFF_MISC + 64;       // tile maxima hand-off, 8 slots x 128 floats
-  static constexpr int SMEM = OFF_MBUF + 4096 + 1024;  // + slack for aligning the base to 1024
-  static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
+  static constexpr int OFF_SKS = OFF_MBUF + 4096;      // the K' block scales in visiting order, nkb floats
+  static constexpr int SMEM = OFF_SKS + 1024;          // + the scale table; + slack for aligning the base to 1024
+  static constexpr int MAX_NKB = 8192;                 // S <= 2^20
+  static_assert(SMEM + 4 * MAX_NKB <= 227 * 1024, "shared memory per CTA");
   static_assert(OFF_V % 1024 == 0 && VSTAGE % 1024 == 0 && OFF_K % 1024 == 0, "128-byte swizzle atoms");
   // A V stage is refilled once PV of its previous tile is complete (o_done): with at most four
   // stages PV(t + 4) needs the tile being loaded, so that barrier cannot run two phases ahead.
@@ -131,6 +133,7 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base + C::OFF_MISC + 8);
   float* mbuf = reinterpret_cast<float*>(base + C::OFF_MBUF);
+  float* sks = reinterpret_cast<float*>(base + C::OFF_SKS);
 
   // The warp index read back from lane 0 is one the compiler knows to be warp-uniform: each role's
   // loop state and the MMA descriptors then live in uniform registers.
@@ -162,6 +165,9 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(tmem_slot, 512);
+  // The K' block scales of this batch-head, in visiting order: the softmax loop then issues no global
+  // load, so none is in flight when its barrier arrivals (releases) execute.
+  for (int p = tid; p < nkb; p += blockDim.x) sks[p] = args.kscales[(int64_t)bh * nkb + tile_at(p, start)];
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -414,7 +420,6 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
     const uint32_t tL = tmem + lane_base + C::T_L;
     const uint32_t tS = tmem + lane_base + C::T_S + 128 * wg;
     const uint32_t tP = tmem + lane_base + (wg ? C::T_P1 : C::T_P0);
-    const float* skh = args.kscales + (int64_t)bh * nkb;
     const float* skr = args.krep_scales + (int64_t)bh * args.nrt;
     const float aq = args.code_scale * args.qscales[(int64_t)bh * nkb + qt];
     // One scale per head: the means are in true units and the flush operand carries 1/sV. Per
@@ -425,7 +430,6 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
     const int tail_valid = args.S - (nkb - 1) * 128;
     bool ok = true;
     int known = -1;  // every PV up to this tile is known complete
-    float sk_next = wg < nkb ? skh[tile_at(wg, start)] : 1.f;
 
     auto wait_o = [&](int t) -> bool {
       if (!warp_wait(&o_done[t & 3], (t >> 2) & 1, kWaitLimit, abort_flag)) {
@@ -466,8 +470,7 @@ __global__ void __launch_bounds__(352, 1) vc_fwd_kernel(const __grid_constant__ 
       if (t >= nkb) break;
       if (warp_aborted(abort_flag)) { ok = false; break; }
       const int j = tile_at(t, start);
-      const float sk = sk_next;
-      if (t + 2 < nkb) sk_next = skh[tile_at(t + 2, start)];
+      const float sk = sks[t];
       const uint32_t lim = (t == 0 && (args.flags & VC_DEBUG_TIMEOUT)) ? 0u : kWaitLimit;
       if (!warp_wait(s_full, k & 1, lim, abort_flag)) {
         record_failure(args.status, abort_flag, kStatusTimeoutS);
@@ -774,7 +777,8 @@ template <int D, bool kExpCast, bool kRepair>
 static int launch_fwd(const PlanBuffers& p, const FwdMaps& maps, uint16_t* O, unsigned flags, cudaStream_t st) {
   using C = FwdCfg<D>;
   static std::atomic<uint64_t> attr_done{0};
-  if (ensure_smem_attr(vc_fwd_kernel<D, kExpCast, kRepair>, C::SMEM, attr_done) != VC_OK) return VC_ERR_CUDA;
+  if (ensure_smem_attr(vc_fwd_kernel<D, kExpCast, kRepair>, C::SMEM + 4 * C::MAX_NKB, attr_done) != VC_OK)
+    return VC_ERR_CUDA;
   FwdArgs a;
   a.qscales = p.qscales;
   a.kscales = p.kscales;
@@ -795,7 +799,8 @@ static int launch_fwd(const PlanBuffers& p, const FwdMaps& maps, uint16_t* O, un
   a.use_mean = (p.has_means && (flags & VC_VSMOOTH)) ? 1 : 0;
   if (a.use_mean && a.nrt > 0) return VC_ERR_INVALID_ARG;  // repair rows exist only without means
   dim3 grid(p.nkb, p.B * p.H);
-  vc_fwd_kernel<D, kExpCast, kRepair><<<grid, 352, C::SMEM, st>>>(maps, a);
+  if (p.nkb > C::MAX_NKB) return VC_ERR_UNSUPPORTED;
+  vc_fwd_kernel<D, kExpCast, kRepair><<<grid, 352, C::SMEM + 4 * ((p.nkb + 3) & ~3), st>>>(maps, a);
   return cudaPeekAtLastError() == cudaSuccess ? VC_OK : VC_ERR_CUDA;
 }
 

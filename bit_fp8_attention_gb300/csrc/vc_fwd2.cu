@@ -45,8 +45,10 @@ struct Fwd2Cfg {
   static constexpr int OFF_BAR = OFF_MU + NMU * MUB;
   static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 2 * NMU + 2 * 5 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + slack for aligning the base to 1024
-  static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
+  static constexpr int OFF_SKS = OFF_MISC + 64;      // the K' block scales in visiting order, nkb floats
+  static constexpr int SMEM = OFF_SKS + 1024;         // + the scale table; + slack for aligning the base to 1024
+  static constexpr int MAX_NKB = 8192;                // S <= 2^20
+  static_assert(SMEM + 4 * MAX_NKB <= 227 * 1024, "shared memory per CTA");
   static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && VSTAGE % 1024 == 0 && QB % 1024 == 0,
                 "swizzle atoms");
   static_assert((SW * D) % 1024 == 0, "a score sub-tile starts on a swizzle atom of the K tile");
@@ -86,6 +88,7 @@ __global__ void __launch_bounds__(352, 1) vc_fwd2_kernel(const __grid_constant__
   uint64_t* drain = f_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base + C::OFF_MISC + 8);
+  float* sks = reinterpret_cast<float*>(base + C::OFF_SKS);
 
   // The warp index read back from lane 0 is one the compiler knows to be warp-uniform: each role's
   // loop state and the MMA descriptors then live in uniform registers.
@@ -115,6 +118,9 @@ __global__ void __launch_bounds__(352, 1) vc_fwd2_kernel(const __grid_constant__
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(tmem_slot, 512);
+  // The K' block scales of this batch-head, in visiting order: the softmax loop then issues no global
+  // load, so none is in flight when its barrier arrivals (releases) execute.
+  for (int p = tid; p < nkb; p += blockDim.x) sks[p] = args.kscales[(int64_t)bh * nkb + tile_at(p, start)];
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -347,7 +353,6 @@ __global__ void __launch_bounds__(352, 1) vc_fwd2_kernel(const __grid_constant__
     const int qt = q0 + g;
     const uint32_t tg = tmem + ((uint32_t)(wq * 32) << 16) + 256 * g;
     const uint32_t tO = tg + C::T_O, tW = tg + C::T_W, tP = tg + C::T_P, tF = tg + C::T_F, tS = tg + C::T_S;
-    const float* skh = args.kscales + (int64_t)bh * nkb;
     const float aq = args.code_scale * (qt < nkb ? args.qscales[(int64_t)bh * nkb + qt] : 1.f);
     // One scale per head: the means are in true units and the flush operand carries 1/sV. Per
     // channel: the means are already divided by the channel scales, and the epilogue applies them.
@@ -396,12 +401,10 @@ __global__ void __launch_bounds__(352, 1) vc_fwd2_kernel(const __grid_constant__
       }
       return true;
     };
-    float sk_next = skh[tile_at(0, start)];
     for (int t = 0; ok && t < nkb; ++t) {
       if (warp_aborted(abort_flag)) { ok = false; break; }
       const int j = tile_at(t, start);
-      const float sk = sk_next;
-      if (t + 1 < nkb) sk_next = skh[tile_at(t + 1, start)];
+      const float sk = sks[t];
       float s[128];
       if (!load_scores(t, s)) { ok = false; break; }
       if (j == nkb - 1 && tail_valid < 128) {  // keys past S: -inf for the max, code 0
@@ -573,7 +576,8 @@ template <int D, bool kExpCast, bool kRepair>
 static int launch_fwd2(const PlanBuffers& p, const FwdMaps& maps, uint16_t* O, unsigned flags, cudaStream_t st) {
   using C = Fwd2Cfg<D>;
   static std::atomic<uint64_t> attr_done{0};
-  if (ensure_smem_attr(vc_fwd2_kernel<D, kExpCast, kRepair>, C::SMEM, attr_done) != VC_OK) return VC_ERR_CUDA;
+  if (ensure_smem_attr(vc_fwd2_kernel<D, kExpCast, kRepair>, C::SMEM + 4 * C::MAX_NKB, attr_done) != VC_OK)
+    return VC_ERR_CUDA;
   FwdArgs a;
   a.qscales = p.qscales;
   a.kscales = p.kscales;
@@ -594,7 +598,8 @@ static int launch_fwd2(const PlanBuffers& p, const FwdMaps& maps, uint16_t* O, u
   a.use_mean = (p.has_means && (flags & VC_VSMOOTH)) ? 1 : 0;
   if (a.use_mean && a.nrt > 0) return VC_ERR_INVALID_ARG;  // repair rows exist only without means
   dim3 grid((p.nkb + 1) / 2, p.B * p.H);
-  vc_fwd2_kernel<D, kExpCast, kRepair><<<grid, 352, C::SMEM, st>>>(maps, a);
+  if (p.nkb > C::MAX_NKB) return VC_ERR_UNSUPPORTED;
+  vc_fwd2_kernel<D, kExpCast, kRepair><<<grid, 352, C::SMEM + 4 * ((p.nkb + 3) & ~3), st>>>(maps, a);
   return cudaPeekAtLastError() == cudaSuccess ? VC_OK : VC_ERR_CUDA;
 }
 
