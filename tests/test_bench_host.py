@@ -18,3 +18,12 @@ def test_cpulist_parser_reads_the_sysfs_format():
 def test_launch_count_per_step_follows_the_rounds():
     # each k-means round launches the assignment, the update and the three argsort kernels
     assert bench.launches_per_step({"iters": 4}) == bench.launches_per_step({"iters": 3}) + 5
+
+
+def test_cpu_baseline_heads_spread_over_the_batch():
+    # the CPU-baseline sample covers heads across the whole range, head 0 first, never past the last
+    assert bench.spread_heads(40, 8) == [0, 5, 10, 15, 20, 25, 30, 35]
+    assert bench.spread_heads(48, 8) == [0, 6, 12, 18, 24, 30, 36, 42]
+    assert bench.spread_heads(3, 8) == [0, 1, 2]
+    assert bench.spread_heads(1, 8) == [0]
+    assert bench.spread_heads(16, 1) == [0]
