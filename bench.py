@@ -91,12 +91,21 @@ def forward_kernel_name(D: int) -> str:
     return "vc_fwd_kernel<128>" if D == 128 else "vc_fwd2_kernel<64>"
 
 
+def code_only(text: str) -> str:
+    """C/CUDA source without its comments and blank lines, each line stripped of surrounding whitespace (the
+    sources contain no comment markers inside string literals)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).strip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def forward_source_hash(D: int = 128) -> str:
-    """First 16 hex digits of the sha256 of the forward kernel's sources (which ncu counters are valid for)."""
+    """First 16 hex digits of the sha256 of the forward kernel's code (the sources without comments), which the
+    committed ncu counters are valid for: a change of comments alone keeps the hash."""
     h = hashlib.sha256()
     for name in (FWD_SOURCES if D == 128 else FWD2_SOURCES):
-        with open(os.path.join(ROOT, "bit_fp8_attention_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "bit_fp8_attention_gb300", "csrc", name), encoding="utf-8") as f:
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

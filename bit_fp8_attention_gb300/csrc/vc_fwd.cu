@@ -9,8 +9,9 @@
 //
 // GB300 design (not the pages' kernel): one CTA per 128-row query tile and batch-head. This kernel serves
 // D = 128; D = 64 runs the two-query-tile kernel of vc_fwd2.cu.
-//   producer    TMA: Q once; K' and V^T tiles of 128 keys into 3-stage rings; with
-//               V-Smooth, the transposed bf16 means of each 16-tile block run into a 2-stage ring.
+//   producers   TMA: Q once; K' tiles of 128 keys two at a time into a 2-stage ring, V^T tiles into
+//               4 stages; with V-Smooth, the transposed bf16 means of each 16-tile block run into a
+//               2-stage ring. The K' block scales of the head sit in shared memory in visiting order.
 //   MMA issuer  one warp, one elected lane issuing: S = Q K'^T for two key tiles at once
 //               (kind::f8f6f4, SS, N = 256) into the two TMEM score buffers; O += P V and
 //               W += P E_{j mod 16} (TS: the codes P are read from TMEM),
@@ -24,12 +25,12 @@
 //               O/W/l rescale on every increase, E4M3 codes written into TMEM.
 //   warp 8      TMA producer of Q and the K pairs; warp 10 TMA producer of V (with the one-hot rows)
 //               and the mean blocks; warp 9 MMA issuer.
-// V residual repair ("Open-VC Attention", "Why V residual repair"): after every regular tile the CTA
+// V residual repair ("Open-VC Attention", "Why V residual repair"): after the regular tiles the CTA
 // visits the plan's repair tiles (copied keys, residual codes) through the same pipeline, with zero
 // one-hot rows (nothing enters W or l) and the running max kept (codes clipped at 120).
 // TMEM columns: O [0, D), W [D, D+16), F [D+16, D+32), l [D+32], P [176, 208) and [208, 240),
-// score buffers S [256, 384) and [384, 512).  P has its own columns so that the commit of S(p+2), which
-// tracks every earlier MMA, also proves that PV(p) has finished reading P(p).
+// score buffers S [256, 384) and [384, 512). P has its own columns, so the commit of score pair k, which
+// tracks every earlier MMA of the issuing thread, also proves that PV(2k-3) has finished reading its P.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>

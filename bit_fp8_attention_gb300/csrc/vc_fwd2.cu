@@ -14,6 +14,8 @@
 //   warp 9      MMA issuer (one elected lane): per key tile, S_g = Q_g K'^T for both groups, in NH
 //               sub-tiles of 128/NH keys (the score buffer of a group holds one sub-tile); then, once a
 //               group's codes are written, its mean term and O_g|W_g += P_g [V; E_{j mod 16}].
+// The K' block scales of the head sit in shared memory in visiting order, so the softmax loop issues no
+// global load.
 // TMEM, group g at column 256 g: O|W [0, D+16), P [D+16, D+48) (the 128 codes of a tile), F [D+48,
 // D+64) (the mean operand), S [256 - 128/NH, 256).  D = 64 fits whole score tiles (NH = 1); D = 128
 // would need NH = 2, measured slower than the one-query-tile kernel, so only D = 64 is launched.

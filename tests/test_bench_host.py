@@ -27,3 +27,11 @@ def test_cpu_baseline_heads_spread_over_the_batch():
     assert bench.spread_heads(3, 8) == [0, 1, 2]
     assert bench.spread_heads(1, 8) == [0]
     assert bench.spread_heads(16, 1) == [0]
+
+
+def test_kernel_hash_ignores_comments_only():
+    # the ncu figures in profiles/ stay attached to the kernel while only its comments change
+    a = "int x = 1;  // one\n/* block\n comment */\n\n  int y = x + 2;\n"
+    b = "// header\nint x = 1;\nint y = x + 2;  /* two */\n"
+    assert bench.code_only(a) == bench.code_only(b) == "int x = 1;\nint y = x + 2;"
+    assert bench.code_only("int x = 2;") != bench.code_only("int x = 1;")
