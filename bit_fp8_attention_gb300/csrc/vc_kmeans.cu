@@ -470,12 +470,17 @@ __global__ void __launch_bounds__(256) kmeans_update_kernel(const uint16_t* __re
     float s[E], e[E];
 #pragma unroll
     for (int q = 0; q < E; ++q) s[q] = e[q] = 0.f;
+    // Eight independent row loads in flight; the row indices of the next eight are fetched (one per
+    // lane, handed out by shuffles) while this batch's rows load, so a batch waits for one memory
+    // latency, not two. The rows are added in order, one after another, as in the plain loop.
+    constexpr int R = 8;
     int m = 0;
-    for (; m + 4 <= n; m += 4) {  // four independent row loads in flight
-      uint32_t w[4][E / 2];
+    int idx = (lane < R && lane < n) ? __ldg(ph + lane) : 0;
+    for (; m + R <= n; m += R) {
+      uint32_t w[R][E / 2];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const uint16_t* r = vh + (int64_t)__ldg(ph + m + u) * D;
+      for (int u = 0; u < R; ++u) {
+        const uint16_t* r = vh + (int64_t)__shfl_sync(0xffffffffu, idx, u) * D;
         if constexpr (E == 4) {
           const uint2 x = __ldg(reinterpret_cast<const uint2*>(r));
           w[u][0] = x.x;
@@ -484,8 +489,9 @@ __global__ void __launch_bounds__(256) kmeans_update_kernel(const uint16_t* __re
           w[u][0] = __ldg(reinterpret_cast<const uint32_t*>(r));
         }
       }
+      idx = (lane < R && m + R + lane < n) ? __ldg(ph + m + R + lane) : 0;
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+      for (int u = 0; u < R; ++u)
 #pragma unroll
         for (int q = 0; q < E / 2; ++q) {
           two_sum_add(s[2 * q], e[2 * q], bf16_to_f32(w[u][q] & 0xFFFFu));
