@@ -362,15 +362,21 @@ def spread_heads(H: int, n: int) -> list[int]:
 
 
 def cpu_baseline(cfg, Q, K, V, rows_per_head: int = 64, max_heads: int = 8, kmeans_heads: int = 2):
-    """The oracle, as it stands, on a bounded sample of the workload, extrapolated to one step: one Lloyd
-    round on `kmeans_heads` heads, quantise/gather/demean and the forward on `rows_per_head` random query
-    rows of up to `max_heads` heads spread over batch 0 (about 15-20 s on 16 cores for the Wan-like
-    workload). Per-head means of the sampled times scale to all B*H heads, rounds and rows."""
+    """The oracle, as it stands, timed on the workload. Small workloads (B*H*S^2 <= 2^24: the tiny config)
+    run whole: every k-means round, the quantise/gather/demean and the forward on
+    every row of every head. Larger ones run a bounded sample, extrapolated to one step: one Lloyd round on
+    `kmeans_heads` heads, quantise/gather/demean and the forward on `rows_per_head` random query rows of up
+    to `max_heads` heads spread over batch 0 (about 15-20 s on 16 cores for the Wan-like workload); per-head
+    means of the sampled times scale to all B*H heads, rounds and rows."""
     import oracle
 
     oracle.build()
     S, D, k = cfg["S"], cfg["D"], cfg["k"]
     n_heads_total = cfg["B"] * cfg["H"]
+    full = n_heads_total * S * S <= (1 << 24) and Q.shape[1] == cfg["H"]  # small workloads: every head, every row
+    if full:
+        rows_per_head, max_heads, kmeans_heads = S, cfg["H"], cfg["H"]
+    rounds = cfg["iters"] if full else 1
     heads = spread_heads(Q.shape[1], max_heads)
     rng = np.random.default_rng(0)
     km, prep_t, fwd_t = [], [], []
@@ -380,7 +386,7 @@ def cpu_baseline(cfg, Q, K, V, rows_per_head: int = 64, max_heads: int = 8, kmea
         q, kk, v = (oracle._u16(t[0, h].cpu()) for t in (Q, K, V))
         if i < kmeans_heads:
             t0 = time.perf_counter()
-            oracle.kmeans(v, k, 1)  # one Lloyd round
+            oracle.kmeans(v, k, rounds)
             km.append(time.perf_counter() - t0)
         t0 = time.perf_counter()
         prep = oracle.prepare_head(q, kk, v, k, cfg["iters"], perm=perm)
@@ -389,7 +395,7 @@ def cpu_baseline(cfg, Q, K, V, rows_per_head: int = 64, max_heads: int = 8, kmea
         t0 = time.perf_counter()
         oracle.forward_head(prep, rows)
         fwd_t.append((time.perf_counter() - t0) / len(rows))
-    t_km = statistics.mean(km) * cfg["iters"] * n_heads_total
+    t_km = statistics.mean(km) * (cfg["iters"] // rounds) * n_heads_total
     t_prep = statistics.mean(prep_t) * n_heads_total
     t_fwd = statistics.mean(fwd_t) * S * n_heads_total
     t_step = t_km + t_prep + t_fwd
@@ -398,10 +404,14 @@ def cpu_baseline(cfg, Q, K, V, rows_per_head: int = 64, max_heads: int = 8, kmea
         "unit": "TFLOP/s",
         "cores": oracle.num_threads(),
         "kind": "oracle",
-        "sample": (f"heads {heads} of batch 0: 1 k-means round on {len(km)} of them (x{cfg['iters']} rounds "
-                   f"x {n_heads_total} heads), quantise/gather/demean on each (x{n_heads_total} heads), forward on "
-                   f"{min(S, rows_per_head)} random query rows of each (x{S} rows x {n_heads_total} heads); "
-                   f"extrapolated step {t_step:.1f} s"),
+        "sample": ((f"whole workload: {cfg['iters']} k-means rounds, quantise/gather/demean and the forward on all "
+                    f"{S} rows, every head of batch 0" + (f" (x{cfg['B']} batches)" if cfg["B"] > 1 else "") +
+                    f"; step {t_step:.1f} s")
+                   if full else
+                   (f"heads {heads} of batch 0: 1 k-means round on {len(km)} of them (x{cfg['iters']} rounds "
+                    f"x {n_heads_total} heads), quantise/gather/demean on each (x{n_heads_total} heads), forward on "
+                    f"{min(S, rows_per_head)} random query rows of each (x{S} rows x {n_heads_total} heads); "
+                    f"extrapolated step {t_step:.1f} s")),
         "extrapolated_step_s": t_step,
     }
 
