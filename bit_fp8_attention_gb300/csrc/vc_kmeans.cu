@@ -136,12 +136,12 @@ __device__ __forceinline__ void fail(int* status, volatile int* abort_flag) {
 // Persistent: CTA b takes work items b, b + gridDim.x, ... (item w = head w / ntp, tokens
 // [256 (w % ntp), 256 (w % ntp) + 256)), so that one item's token tiles load while the previous item
 // computes. Local item i uses token buffer i % 2; the c-th chunk this CTA consumes, counted over all
-// its items, uses accumulator buffer c % 2, and its parts (hi, lo) are the stage loads u = 2c, 2c + 1
-// (stage u % NST).
+// its items, uses accumulator buffer c % 2, and its nparts parts (hi, then lo when nparts = 2) are the
+// stage loads u = nparts c, ..., nparts c + nparts - 1 (stage u % NST).
 template <int D>
 __global__ void __launch_bounds__(352, 1)
     kmeans_assign_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap cmap,
-                         const float* __restrict__ cnormp, int S, int kpad, int nwork,
+                         const float* __restrict__ cnormp, int S, int kpad, int nwork, int nparts,
                          int32_t* __restrict__ labels, int* __restrict__ status) {
   using C = AsgCfg<D>;
   extern __shared__ uint8_t asg_smem_raw[];
@@ -214,8 +214,8 @@ __global__ void __launch_bounds__(352, 1)
       for (int i = 0; ok && i < nitems; ++i) {
         const int bh = (blockIdx.x + i * gridDim.x) / ntp;
         for (int ch = 0; ok && ch < nch; ++ch)
-          for (int part = 0; part < 2; ++part) {
-            const int u = 2 * (i * nch + ch) + part, s = u % C::NST;
+          for (int part = 0; part < nparts; ++part) {
+            const int u = nparts * (i * nch + ch) + part, s = u % C::NST;
             if (!wait_or_abort(&c_empty[s], ((u / C::NST) & 1) ^ 1, abort_flag)) { ok = false; break; }
             mbar_arrive_expect_tx(&c_full[s], C::CB);
             for (int h = 0; h < C::HALVES; ++h)
@@ -247,8 +247,8 @@ __global__ void __launch_bounds__(352, 1)
       for (int ch = 0; ok && ch < nch; ++ch) {
         const int c = i * nch + ch, b = c & 1;
         if (!wwait(&acc_empty[b], ((c >> 1) & 1) ^ 1)) { ok = false; break; }
-        for (int part = 0; part < 2; ++part) {
-          const int u = 2 * c + part, s = u % C::NST;
+        for (int part = 0; part < nparts; ++part) {
+          const int u = nparts * c + part, s = u % C::NST;
           if (!wwait(&c_full[s], (u / C::NST) & 1)) { ok = false; break; }
           tc_fence_after();
           if (leader) {
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(352, 1)
               }
             }
             mma_commit(&c_empty[s]);
-            if (part == 1) {
+            if (part == nparts - 1) {
               mma_commit(&acc_full[b]);
               if (ch == nch - 1) mma_commit(&x_empty[xb]);  // the item's token tiles are no longer read
             }
@@ -551,7 +551,11 @@ int launch_kmeans(const PlanBuffers& p, const uint16_t* V, int iters, bool warm,
   // Warm start: the centroids of the plan's previous grouping (and their splits and norms) stay.
   if (!warm) kmeans_init_kernel<D><<<gc, 256, 0, st>>>(V, S, k, kpad, p.cent, p.cnorm, p.cent16, p.cnormp);
   for (int it = 0; it < iters; ++it) {
-    kmeans_assign_kernel<D><<<ga, 352, C::SMEM, st>>>(xmap, cmap, p.cnormp, S, kpad, nwork, p.labels, p.status);
+    // The first round of a cold start compares with data rows, whose lo halves are exactly zero: the
+    // hi halves alone give the same dot products, so that round reads and multiplies only those.
+    const int nparts = (it == 0 && !warm) ? 1 : 2;
+    kmeans_assign_kernel<D><<<ga, 352, C::SMEM, st>>>(xmap, cmap, p.cnormp, S, kpad, nwork, nparts, p.labels,
+                                                      p.status);
     label_hist_kernel<<<gh, 256, 0, st>>>(p.labels, S, k, p.nchunk, p.chist);
     label_scan_kernel<<<BH, 1024, 0, st>>>(k, p.nchunk, p.chist, p.counts, p.offsets);
     label_scatter_kernel<<<gh, 256, 0, st>>>(p.labels, S, k, p.nchunk, p.chist, p.perm);
