@@ -7,12 +7,13 @@
 //
 // GB300 design:
 //   assignment  tcgen05 (kind::f16), persistent (one CTA per SM): per work item two 128-token
-//               tiles of V (bf16, exact) against the centroids in chunks of 64, each centroid split
-//               into bf16 hi + lo (about 16 significant bits); fp32 dot products accumulate in TMEM
-//               (two tiles x two chunk buffers = 256 columns), eight epilogue warps scan the columns
-//               in ascending order for argmin ||c||^2 - 2 x.c. One warp loads the token tiles by TMA
-//               (double-buffered, so the next item's tiles land while this one computes), one the
-//               centroid chunks, and one elected thread issues the MMAs.
+//               tiles of V (bf16, exact) against the centroids in chunks of 128, each centroid split
+//               into bf16 hi + lo (about 16 significant bits) streamed as separate stages; fp32 dot
+//               products accumulate in TMEM (two tiles x two chunk buffers = 512 columns), eight
+//               epilogue warps scan the columns in ascending order for argmin ||c||^2 - 2 x.c. One
+//               warp loads the token tiles by TMA (double-buffered, so the next item's tiles land
+//               while this one computes), one the centroid chunks, and one elected thread issues the
+//               MMAs. A cold start's first round skips the lo halves, which are zero for data rows.
 //   argsort     stable counting sort in three launches: per-chunk label histograms, a scan over
 //               chunks and bins, then a scatter in token order within each chunk.
 //   update      one warp per cluster, compensated fp32 sums (TwoSum) of the member rows read
