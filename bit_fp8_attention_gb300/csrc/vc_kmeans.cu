@@ -362,12 +362,20 @@ __global__ void __launch_bounds__(1024) label_scan_kernel(int k, int nchunk, int
   __shared__ int warp_tot[32];
   const int bh = blockIdx.x, i = threadIdx.x, lane = i & 31, w = i >> 5;
   int32_t* hh = hist + (int64_t)bh * nchunk * k;
+  // Eight chunks' counts are loaded before any of them is overwritten, so each group of eight costs one
+  // memory latency instead of eight.
+  constexpr int G = 8;
   int run = 0;
   if (i < k)
-    for (int c = 0; c < nchunk; ++c) {
-      const int n = hh[(int64_t)c * k + i];
-      hh[(int64_t)c * k + i] = run;
-      run += n;
+    for (int c0 = 0; c0 < nchunk; c0 += G) {
+      int n[G];
+#pragma unroll
+      for (int u = 0; u < G; ++u) n[u] = c0 + u < nchunk ? hh[(int64_t)(c0 + u) * k + i] : 0;
+#pragma unroll
+      for (int u = 0; u < G; ++u) {
+        if (c0 + u < nchunk) hh[(int64_t)(c0 + u) * k + i] = run;
+        run += n[u];
+      }
     }
   // exclusive scan of the totals over the clusters
   int incl = run;
@@ -392,7 +400,14 @@ __global__ void __launch_bounds__(1024) label_scan_kernel(int k, int nchunk, int
   if (i < k) {
     counts[(int64_t)bh * k + i] = run;
     offsets[(int64_t)bh * k + i] = off;
-    for (int c = 0; c < nchunk; ++c) hh[(int64_t)c * k + i] += off;
+    for (int c0 = 0; c0 < nchunk; c0 += G) {
+      int n[G];
+#pragma unroll
+      for (int u = 0; u < G; ++u) n[u] = c0 + u < nchunk ? hh[(int64_t)(c0 + u) * k + i] : 0;
+#pragma unroll
+      for (int u = 0; u < G; ++u)
+        if (c0 + u < nchunk) hh[(int64_t)(c0 + u) * k + i] = n[u] + off;
+    }
   }
 }
 
